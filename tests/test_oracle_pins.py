@@ -1,0 +1,326 @@
+"""Pins for the fp64 oracle: facts fixed by the method and by mathematics,
+not by re-running the oracle's own formulas.
+
+Each test is chosen so that a plausible slip in the oracle -- a dropped
+decay, a wrong sign, a transposed outer product, a wrong GQA index, an
+off-by-one in the align-mode block arithmetic -- fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._tol import bf16_ulp
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+# ------------------------------------------------------------------ gates
+@pytest.mark.parametrize("x", [-30.0, -3.0, -0.5, 0.0, 0.7, 4.0, 30.0])
+@pytest.mark.parametrize("A_log", [0.0, math.log(3.0), math.log(16.0)])
+def test_decay_closed_form(x, A_log):
+    # exp(-c * log(1 + e^x)) == (1 + e^x)^(-c): a different evaluation route.
+    c = math.exp(A_log)
+    expect = (1.0 + math.exp(x)) ** (-c)
+    got = oracle.decay(x - 0.25, A_log, 0.25)   # the gate adds dt_bias to a
+    assert got == pytest.approx(expect, rel=1e-12, abs=1e-300)
+
+
+def test_decay_special_values():
+    assert oracle.decay(0.0, 0.0, 0.0) == pytest.approx(0.5, rel=1e-15)
+    # softplus -> 0 exactly for very negative inputs: the identity decay
+    assert oracle.decay(-1e4, 0.3, 0.0) == 1.0
+    # the decay is a contraction for any input
+    for a in np.linspace(-20, 20, 41):
+        assert 0.0 <= oracle.decay(a, 1.0, 0.5) <= 1.0
+
+
+def test_softplus_closed_forms():
+    assert oracle.softplus(0.0) == pytest.approx(math.log(2.0), rel=1e-15)
+    for c in (1e-3, 0.5, 2.0, 10.0):
+        assert oracle.softplus(math.log(math.expm1(c))) == pytest.approx(c, rel=1e-12)
+    assert oracle.softplus(800.0) == 800.0           # no overflow
+    assert oracle.softplus(-800.0) == 0.0
+    assert oracle.softplus(-30.0) == pytest.approx(math.exp(-30.0), rel=1e-12)
+
+
+def test_beta_closed_forms():
+    assert oracle.beta(0.0) == 0.5
+    assert oracle.beta(math.log(3.0)) == pytest.approx(0.75, rel=1e-15)
+    assert oracle.beta(-math.log(3.0)) == pytest.approx(0.25, rel=1e-15)
+    assert oracle.beta(1e4) == 1.0
+    assert oracle.beta(-1e4) == 0.0
+
+
+def test_l2norm():
+    assert np.allclose(oracle.l2norm([3.0, 4.0]), [0.6, 0.8], rtol=0, atol=1e-7)
+    # eps sits under the square root: |l2norm(x)|^2 = s / (s + eps) with
+    # s = |x|^2, so a vector with s = eps comes out with squared norm 1/2.
+    y = oracle.l2norm([1e-3, 0.0])
+    assert float(y @ y) == pytest.approx(0.5, rel=1e-12)
+    assert np.array_equal(oracle.l2norm(np.zeros(8)), np.zeros(8))
+    x = rng.normal(size=128)
+    y = oracle.l2norm(x)
+    assert np.linalg.norm(y) == pytest.approx(1.0, abs=1e-7)
+    assert np.allclose(y / np.linalg.norm(y), x / np.linalg.norm(x), rtol=0, atol=1e-15)
+
+
+# ------------------------------------------------------- one-unit recurrence
+def test_worked_example_golden():
+    with open(os.path.join(GOLDEN, "worked_example_two_tokens.json")) as f:
+        g = json.load(f)
+    r = oracle.window(g["S0"], g["q"], g["k"], g["v"], g["a"], g["b"], g["A_log"], g["dt_bias"])
+    tol = g["atol"]
+    assert np.allclose(r["alpha"], g["expect_alpha"], rtol=0, atol=1e-15)
+    assert np.allclose(r["u"], g["expect_u"], rtol=0, atol=tol)
+    assert np.allclose(r["states"], g["expect_states"], rtol=0, atol=tol)
+    assert np.allclose(r["o"], g["expect_o"], rtol=0, atol=tol)
+    assert np.allclose(r["khat"], np.array(g["k"]) / math.sqrt(1.0 + 1e-6), rtol=0, atol=1e-15)
+
+
+def _random_unit(K=16, V=16, w=5, seed=0):
+    g = np.random.default_rng(seed)
+    return dict(S0=g.normal(0, 0.1, (V, K)), q=g.normal(size=(w, K)), k=g.normal(size=(w, K)),
+                v=g.normal(size=(w, V)), a=g.normal(size=w), b=g.normal(size=w),
+                A_log=float(g.uniform(0, math.log(16))), dt_bias=float(g.uniform(-1, 1)))
+
+
+def test_identity_gate_leaves_state_unchanged():
+    u = _random_unit()
+    w = len(u["a"])
+    r = oracle.window(u["S0"], u["q"], u["k"], u["v"], np.full(w, -1e4), np.full(w, -1e4),
+                      u["A_log"], 0.0)
+    for t in range(w):
+        assert np.array_equal(r["states"][t], u["S0"])           # bit for bit
+        qh = oracle.l2norm(u["q"][t])
+        assert np.allclose(r["o"][t], u["S0"] @ qh, rtol=1e-13, atol=1e-15)
+    assert np.array_equal(r["u"], np.zeros_like(r["u"]))
+    assert np.array_equal(r["alpha"], np.ones(w))
+
+
+def test_zero_state_single_token_is_rank_one():
+    # S0 = 0: S1 = beta * v khat^T and o1 = beta * (khat . qhat) * v.
+    u = _random_unit(K=8, V=12, w=1, seed=3)
+    r = oracle.window(np.zeros((12, 8)), u["q"], u["k"], u["v"], u["a"], u["b"],
+                      u["A_log"], u["dt_bias"])
+    be = 1.0 / (1.0 + math.exp(-u["b"][0]))
+    kh, qh = oracle.l2norm(u["k"][0]), oracle.l2norm(u["q"][0])
+    assert np.allclose(r["states"][0], be * np.outer(u["v"][0], kh), rtol=1e-13, atol=1e-15)
+    assert np.allclose(r["o"][0], be * float(kh @ qh) * u["v"][0], rtol=1e-12, atol=1e-14)
+
+
+def test_write_invariant_full_strength():
+    # beta = 1: after each token the state maps the (normalised) key onto
+    # its value, S_t khat_t = v_t, up to |khat|^2 = 1 - eps/(|k|^2 + eps).
+    u = _random_unit(K=32, V=24, w=6, seed=5)
+    w = len(u["a"])
+    r = oracle.window(u["S0"], u["q"], u["k"], u["v"], u["a"], np.full(w, 1e4),
+                      u["A_log"], u["dt_bias"])
+    for t in range(w):
+        kh = oracle.l2norm(u["k"][t])
+        assert np.allclose(r["states"][t] @ kh, u["v"][t], rtol=0, atol=1e-6)
+
+
+def test_orthonormal_keys_store_exact_memories():
+    # alpha = 1, beta = 1, keys = distinct basis vectors: the delta rule
+    # writes each value into its key's column and leaves the rest alone:
+    # S_n = S0 + sum_t (v_t - S0 e_t) e_t^T.
+    K, V, w = 10, 7, 4
+    g = np.random.default_rng(7)
+    S0 = g.normal(0, 0.1, (V, K))
+    cols = [3, 0, 8, 5]
+    k = np.zeros((w, K)); k[np.arange(w), cols] = 2.5      # scale is removed by the norm
+    v = g.normal(size=(w, V)); q = g.normal(size=(w, K))
+    r = oracle.window(S0, q, k, v, np.full(w, -1e4), np.full(w, 1e4), 0.0, 0.0)
+    expect = S0.copy()
+    for t, c in enumerate(cols):
+        expect[:, c] = v[t]
+    assert np.allclose(r["states"][-1], expect, rtol=0, atol=1e-6)
+
+
+def test_pure_decay():
+    # beta = 0: S_n = (prod alpha_t) S0, with alpha from the closed form.
+    u = _random_unit(w=4, seed=9)
+    r = oracle.window(u["S0"], u["q"], u["k"], u["v"], u["a"], np.full(4, -1e4),
+                      u["A_log"], u["dt_bias"])
+    c = math.exp(u["A_log"])
+    prod = 1.0
+    for t in range(4):
+        prod *= (1.0 + math.exp(u["a"][t] + u["dt_bias"])) ** (-c)
+        assert np.allclose(r["states"][t], prod * u["S0"], rtol=1e-12, atol=1e-300)
+
+
+def test_replay_from_record_equals_recompute():
+    u = _random_unit(K=16, V=16, w=6, seed=11)
+    r = oracle.window(u["S0"], u["q"], u["k"], u["v"], u["a"], u["b"], u["A_log"], u["dt_bias"])
+    assert np.array_equal(oracle.replay(u["S0"], r["u"][:0], r["khat"][:0], r["alpha"][:0]),
+                          u["S0"])
+    for n in range(1, 7):
+        S = oracle.replay(u["S0"], r["u"][:n], r["khat"][:n], r["alpha"][:n])
+        assert np.allclose(S, r["states"][n - 1], rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------- align-mode plan
+def _brute_force_writes(p0, n, Bk):
+    """Walk the accepted tokens one by one: the block of token x (1-based
+    position) ends up holding the state after the last accepted token that
+    falls in it.  Returns {column: tokens folded}."""
+    cols = {}
+    for x in range(p0 + 1, p0 + n + 1):
+        cols[(x - 1) // Bk] = x - p0
+    return cols
+
+
+@pytest.mark.parametrize("Bk", [1, 2, 3, 4, 8])
+def test_align_plan_matches_brute_force(Bk):
+    W = 6
+    for p0 in range(1, 4 * Bk + 1):
+        ncols = (p0 + W - 1) // Bk + 1
+        table = [100 + c for c in range(ncols)]   # column c -> slot 100 + c
+        for n in range(0, W + 1):
+            src, writes = oracle.commit_plan(W, n, table, p0, Bk, 1000, W)
+            assert src == table[(p0 - 1) // Bk]
+            got = {s - 100: t for s, t in writes}
+            assert len(got) == len(writes), "a slot written twice"
+            assert got == _brute_force_writes(p0, n, Bk), (p0, n)
+            if writes:
+                assert writes[0] == (table[(p0 + n - 1) // Bk], n)   # final first
+
+
+def test_plan_without_align_mode_updates_in_place():
+    for n in range(0, 5):
+        src, writes = oracle.commit_plan(4, n, [42], 0, 0, 64, 4)
+        assert src == 42
+        assert writes == ([] if n == 0 else [(42, n)])
+
+
+def test_plan_null_and_errors():
+    assert oracle.commit_plan(4, 2, [-1], 0, 0, 8, 4) == (-1, [])          # null slot
+    assert oracle.commit_plan(0, 0, [3], 0, 0, 8, 4) == (-1, [])           # empty window
+    with pytest.raises(ValueError) as e:
+        oracle.commit_plan(4, 5, [3], 0, 0, 8, 4)
+    assert e.value.args[0] == oracle.ERR_ACCEPTED
+    with pytest.raises(ValueError) as e:
+        oracle.commit_plan(5, 1, [3], 0, 0, 8, 4)
+    assert e.value.args[0] == oracle.ERR_WINDOW
+    with pytest.raises(ValueError) as e:
+        oracle.commit_plan(4, 1, [8], 0, 0, 8, 4)
+    assert e.value.args[0] == oracle.ERR_SLOT
+    with pytest.raises(ValueError) as e:            # align: final block missing
+        oracle.commit_plan(4, 2, [5, -1], 4, 4, 8, 4)
+    assert e.value.args[0] == oracle.ERR_BLOCK
+    with pytest.raises(ValueError) as e:            # align: column beyond the table
+        oracle.commit_plan(4, 2, [5], 4, 4, 8, 4)
+    assert e.value.args[0] == oracle.ERR_BLOCK
+    with pytest.raises(ValueError) as e:
+        oracle.commit_plan(4, 2, [5, 6], 0, 4, 8, 4)
+    assert e.value.args[0] == oracle.ERR_SEQPOS
+
+
+# ------------------------------------------------------------ batch level
+def _batch(HK=2, HV=4, K=8, V=8, W=4, windows=(4, 2, 0, 3, 2), slots=(0, 2, -1, 3, -1), seed=0):
+    g = np.random.default_rng(seed)
+    B = len(windows)
+    starts = np.cumsum([0] + list(windows[:-1])).astype(np.int32)
+    T = int(sum(windows))
+    return dict(q=g.normal(size=(T, HK, K)), k=g.normal(size=(T, HK, K)),
+                v=g.normal(size=(T, HV, V)), a=g.normal(size=(T, HV)), b=g.normal(size=(T, HV)),
+                A_log=g.uniform(0, math.log(16), HV), dt_bias=g.uniform(-1, 1, HV),
+                token_start=starts, window_len=np.array(windows, np.int32),
+                pool=g.normal(0, 0.1, (5, HV, V, K)), slot_table=np.array(slots, np.int32),
+                max_window=W)
+
+
+def test_gqa_uses_consecutive_key_groups():
+    # HV = 2 * HK: value heads 2j and 2j+1 read key head j.  Expanding the
+    # keys/queries to one per value head with repeat_interleave must give
+    # the same result as the grouped run.
+    d = _batch()
+    grouped = oracle.spec_verify(**d)
+    e = dict(d)
+    e["q"] = np.repeat(d["q"], 2, axis=1)
+    e["k"] = np.repeat(d["k"], 2, axis=1)
+    expanded = oracle.spec_verify(**e)
+    for key in ("out", "rec_u", "rec_k", "rec_g"):
+        assert np.array_equal(grouped[key], expanded[key], equal_nan=True), key
+    e["q"] = np.tile(d["q"], (1, 2, 1))        # the other plausible mapping differs
+    e["k"] = np.tile(d["k"], (1, 2, 1))
+    tiled = oracle.spec_verify(**e)
+    assert not np.allclose(np.nan_to_num(grouped["out"]), np.nan_to_num(tiled["out"]))
+
+
+def test_verify_writes_only_live_rows():
+    d = _batch()
+    r = oracle.spec_verify(**d, snapshots=True)
+    assert np.all(r["row_err"] == 0)
+    starts, windows = d["token_start"], d["window_len"]
+    for row, (s, w) in enumerate(zip(starts, windows)):
+        live = w > 0 and d["slot_table"][row] >= 0
+        blk = r["out"][s:s + w]
+        assert np.all(np.isfinite(blk)) if live else np.all(np.isnan(blk))
+        rec = r["rec_u"][row, :, :w]
+        assert np.all(np.isfinite(rec)) if live else np.all(np.isnan(rec))
+        assert np.all(np.isnan(r["rec_u"][row, :, w:]))      # beyond the window
+        assert np.all(np.isnan(r["snaps"][row, w:]))
+
+
+def test_commit_equals_native_snapshot_states():
+    # Commit after n accepted tokens (replay from records) equals the
+    # recomputed state after n tokens, for every n, and writes only the
+    # final slot; slots of null rows stay unchanged.
+    d = _batch()
+    B = len(d["window_len"])
+    v = oracle.spec_verify(**d, snapshots=True)
+    for n_first in range(0, 5):
+        acc = np.array([n_first, 2, 0, 1, 2], np.int32)
+        pools, err = oracle.replay_commit(
+            pools=d["pool"][None], rec_u=v["rec_u"][None], rec_k=v["rec_k"][None],
+            rec_g=v["rec_g"][None], window_len=d["window_len"], accepted_len=acc,
+            slot_table=d["slot_table"], max_window=4)
+        assert np.all(err == 0)
+        expect = d["pool"].copy()
+        for r in range(B):
+            s, n = d["slot_table"][r], acc[r]
+            if s >= 0 and n > 0:
+                expect[s] = v["snaps"][r, n - 1]
+        assert np.allclose(pools[0], expect, rtol=1e-12, atol=1e-14)
+
+
+def test_config_tiny_checkpoint_untouched_and_consistent():
+    from spec_decode_recurrent_gb300 import workloads
+    sb = workloads.tiny()
+    pool = sb.pools[0].clone()
+    r = oracle.spec_verify(q=sb.q[0], k=sb.k[0], v=sb.v[0], a=sb.a[0], b=sb.b[0],
+                           A_log=sb.A_log[0], dt_bias=sb.dt_bias[0],
+                           token_start=sb.token_start, window_len=sb.window_len,
+                           pool=sb.pools[0], slot_table=sb.slot_table, max_window=sb.W,
+                           snapshots=True)
+    assert torch.equal(pool.view(torch.int32), sb.pools[0].view(torch.int32))
+    assert np.all(np.isfinite(r["out"])) and np.all(np.isfinite(r["rec_u"]))
+    # The normalised key in the record has unit norm (up to eps).
+    assert np.allclose(np.linalg.norm(r["rec_k"], axis=-1), 1.0, atol=1e-6)
+
+
+# ------------------------------------------------------------- bf16 grid
+def test_bf16_ulp_values():
+    assert bf16_ulp(1.0) == 2.0 ** -7
+    assert bf16_ulp(1.99) == 2.0 ** -7
+    assert bf16_ulp(2.0) == 2.0 ** -6
+    assert bf16_ulp(0.1) == 2.0 ** -11
+    assert bf16_ulp(-3.0) == 2.0 ** -6
+    assert bf16_ulp(0.0) == 2.0 ** -133
+
+
+def test_bf16_ulp_is_grid_spacing():
+    x = torch.tensor(rng.normal(0, 0.3, 4096), dtype=torch.float32)
+    xb = x.to(torch.bfloat16)
+    nxt = (xb.view(torch.int16) + 1).view(torch.bfloat16)   # next value away from zero
+    spacing = (nxt.double() - xb.double()).abs().numpy()
+    assert np.array_equal(spacing, bf16_ulp(xb.double().numpy()))
+    assert np.all(np.abs(xb.double().numpy() - x.double().numpy())
+                  <= 0.5 * bf16_ulp(xb.double().numpy()) + 0.0)
