@@ -1,0 +1,477 @@
+#!/usr/bin/env python
+"""Benchmark: GDN speculative verify + all-layer replay commit on one GB300.
+
+A step is one pass of the whole hot path over one batch: the verify of
+every GDN layer (one launch per layer, replayed from a CUDA graph captured
+from the public API calls, as a serving engine runs its forward) followed by
+the single all-layer commit launch (called eagerly, outside the graph, as an
+engine commits after sampling).  Inputs are resident in HBM; one step
+touches far more bytes than the 129 MB L2, so no flush is needed.
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from spec_decode_recurrent_gb300 import api, build, dist, roofline, step, workloads  # noqa: E402
+
+METRIC = "GDN verify+all-layer commit µs/step and achieved HBM GB/s vs ~8 TB/s roofline"
+UNIT = "us/step"
+
+DESCR = {
+    "all_layer": "36 GDN layers, batch 64 (56 live rows + 8 graph-padding rows with null slot "
+                 "and window 0), HK=16 HV=32 K=V=128, window 4 (MTP 3), accepted uniform 1..4, "
+                 "bf16 q/k/v, fp32 [V,K] state, slots a random permutation of a 256-slot pool, seed 2",
+    "layer": "1 GDN layer at serving shape, batch 16, HK=16 HV=32 K=V=128, window 4, "
+             "accepted uniform 1..4, bf16 q/k/v, fp32 state, seed 1",
+    "long_ragged": "36 GDN layers, batch 256, window 6 mixed with ragged 4/1/3, permuted "
+                   "non-contiguous rows, strided fused q/k/v, gates U(-20,20), 512-slot pools, seed 30",
+    "align": "36 GDN layers, batch 128, window 4, align mode with block size 4, boundary "
+             "slot often equal to the source slot, 384-slot pools, seed 4",
+}
+
+
+def parse():
+    p = argparse.ArgumentParser(description=__doc__)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=500)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--workload", choices=sorted(DESCR), default="all_layer")
+    p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
+    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="CPU time budget of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layers", type=int, default=None,
+                   help="fewer layers (for small profiler captures; not a bench line)")
+    return p.parse_args()
+
+
+def make_workload(name, device, rank, state_dtype, layers=None):
+    fn = workloads.WORKLOADS[name]
+    kw = dict(device=device, sentinel=False)
+    if layers is not None:
+        kw["L"] = layers
+    base = {"all_layer": 2, "layer": 1, "long_ragged": 30, "align": 4}[name]
+    kw["seed"] = dist.replica_seed(base, rank)
+    if name in ("all_layer", "align") and state_dtype == torch.bfloat16:
+        kw["state_dtype"] = state_dtype
+    return fn(**kw)
+
+
+# --------------------------------------------------------------- clocks
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device):
+        self.proc = None
+        self.file = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.gpu_id = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            cols = [c.strip() for c in line.split(",")]
+            if len(cols) < 9:
+                continue
+            try:
+                sm.append(float(cols[1]))
+                smax.append(float(cols[2]))
+                power.append(float(cols[3]))
+            except ValueError:
+                continue
+            for n, c in zip(names, cols[5:9]):
+                if c.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+COMMIT_SOURCES = ["spec_decode_recurrent_gb300/csrc/gdn_commit.cu",
+                  "spec_decode_recurrent_gb300/csrc/gdn_device.cuh"]
+
+
+def profiled_traffic(workload, sources):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    from the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"commit_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != source_hash(sources):
+        return None
+    return float(t.group(1))
+
+
+# ---------------------------------------------------------- the GPU arm
+def run_gpu(args, rank, local_rank, world_size):
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    build.build()
+    api.load()
+    sd = torch.bfloat16 if args.state_dtype == "bf16" else torch.float32
+    sb = make_workload(args.workload, dev, rank, sd, args.layers)
+    bufs = step.StepBuffers(sb)
+    stream = torch.cuda.current_stream()
+
+    # eager warm-up (loads the kernels), then capture the verify of all layers
+    for _ in range(2):
+        step.verify_all(sb, bufs)
+        step.commit(sb, bufs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.verify_all(sb, bufs)
+    torch.cuda.synchronize()
+
+    def one_step():
+        graph.replay()
+        step.commit(sb, bufs)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(dev)
+    clocks.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+        step.commit(sb, bufs)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    dist.barrier()
+    clk = clocks.stop()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    verify_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    commit_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    assert int(bufs.err.item()) == 0, "row errors in the benchmark workload"
+    total_ms = dist.max_over_ranks(total_ms, dev)
+    ms_per_step = total_ms / K
+
+    commit_us = statistics.mean(commit_ms) * 1e3
+    verify_us_layer = statistics.mean(verify_ms) * 1e3 / sb.L
+    cbytes = roofline.commit_bytes(sb)
+    vbytes = roofline.verify_bytes_per_layer(sb)
+    peak, peak_kind = measured_peaks()
+    achieved = cbytes / (commit_us * 1e-6) / 1e9
+    v_achieved = vbytes / (verify_us_layer * 1e-6) / 1e9
+
+    # native per-draft-snapshot baseline of one layer (the comparison, not the step)
+    out_n, snaps = step.native_buffers(sb)
+    for _ in range(3):
+        step.native_layer(sb, 0, out_n, snaps)
+    torch.cuda.synchronize()
+    n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(sb.L, 8)
+    n0.record(stream)
+    for i in range(reps):
+        step.native_layer(sb, i % sb.L, out_n, snaps)
+    n1.record(stream)
+    torch.cuda.synchronize()
+    native_us = n0.elapsed_time(n1) * 1e3 / reps
+    nbytes = roofline.native_bytes_per_layer(sb)
+    del out_n, snaps
+
+    e2e = None if args.no_e2e else run_e2e(args, sb, bufs, graph, stream)
+
+    result = {
+        "metric": METRIC, "value": round(ms_per_step * 1e3, 3), "unit": UNIT,
+        "n_gpus": world_size, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; see workloads.py)",
+        "config": {
+            "workload": f"{args.workload}: {DESCR[args.workload]}",
+            "layers": sb.L, "batch": sb.B, "heads_k": sb.HK, "heads_v": sb.HV,
+            "head_k": sb.K, "head_v": sb.V, "window": sb.W,
+            "state_dtype": args.state_dtype, "qkv_dtype": "bf16" if sb.qkv_dtype == torch.bfloat16 else "f32",
+            "parallelism": f"replicas x{world_size} (no collective on the path)",
+            "l2": f"no flush: inputs larger than L2 ({(cbytes + vbytes * sb.L) / 1e9:.1f} GB of "
+                  f"algorithmic traffic per step vs 0.13 GB L2)",
+            "step": "verify of every layer (CUDA graph of the per-layer API calls) + one "
+                    "all-layer commit call",
+        },
+        "roofline": {
+            "kernel": "gdn_commit_kernel (all-layer replay commit)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+            "traffic": profiled_traffic(args.workload, COMMIT_SOURCES),
+            "algorithmic_bytes_per_launch": cbytes, "launch_us": round(commit_us, 2),
+        },
+        "verify": {
+            "kernel": "gdn_verify_kernel", "us_per_layer": round(verify_us_layer, 2),
+            "algorithmic_bytes_per_layer": vbytes, "achieved_gbs": round(v_achieved, 1),
+            "frac": round(v_achieved / peak, 4),
+        },
+        "native_snapshot": {
+            "kernel": "gdn_verify_kernel<native>", "us_per_layer": round(native_us, 2),
+            "algorithmic_bytes_per_layer": nbytes,
+            "achieved_gbs": round(nbytes / (native_us * 1e-6) / 1e9, 1),
+            "note": "comparison baseline, not part of the step",
+        },
+        "gpu_launches": K * (sb.L + 1),
+        "clocks": clk,
+        "wall_s_timed": round(wall, 3),
+    }
+    if e2e:
+        result["e2e"] = e2e
+    if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(sb, args.cpu_seconds)
+    return result
+
+
+def run_e2e(args, sb, bufs, graph, stream):
+    """The same step through the public API with host buffers: every step
+    copies its inputs from pinned host memory, runs, and reads back the
+    outputs of every layer and the error word."""
+    ins = []
+    for l in range(sb.L):
+        srcs = sb.fused_qkv[l:l + 1] if sb.fused_qkv else [sb.q[l], sb.k[l], sb.v[l]]
+        for t in srcs + [sb.a[l], sb.b[l]]:
+            ins.append(t)
+    ins += [sb.token_start, sb.window_len, sb.accepted_len, sb.slot_table]
+    if sb.seq_pos is not None:
+        ins.append(sb.seq_pos)
+    host_in = [t.cpu().pin_memory() for t in ins]
+    outs = bufs.out + [bufs.err]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    bi = sum(t.numel() * t.element_size() for t in host_in)
+    bo = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        for d, h in zip(ins, host_in):
+            d.copy_(h, non_blocking=True)
+        graph.replay()
+        step.commit(sb, bufs)
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    dist.barrier()
+    E = max(1, args.e2e_steps)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(E):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max_over_ranks(a.elapsed_time(b), torch.cuda.current_device()) / E
+    return {"value": round(ms * 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "steps": E,
+            "path": "pinned host -> device copies, verify graph + commit call, device -> host "
+                    "copies of every layer's output and the error word"}
+
+
+# ---------------------------------------------------- CPU oracle timing
+def _compact_layer(sb, l, rows):
+    """Host copies of one layer restricted to `rows`, with the pool reduced
+    to the slots those rows read and write (the oracle's input; not timed)."""
+    import numpy as np
+    table = sb.slot_table[rows].cpu()
+    used = sorted({int(s) for s in table.flatten().tolist() if s >= 0})
+    remap = {s: i for i, s in enumerate(used)}
+    new_table = table.clone()
+    for i in range(new_table.shape[0]):
+        for j in range(new_table.shape[1]):
+            s = int(new_table[i, j])
+            new_table[i, j] = remap[s] if s >= 0 else -1
+    win = sb.window_len[rows].cpu()
+    start = sb.token_start[rows].cpu()
+    # gather each row's token rows contiguously
+    tok = [int(start[i]) + t for i in range(len(rows)) for t in range(int(win[i]))]
+    new_start = torch.tensor(np.concatenate([[0], np.cumsum(win.numpy())[:-1]]), dtype=torch.int32)
+    idx = torch.tensor(tok, dtype=torch.long, device=sb.device)
+    f64 = lambda t: np.ascontiguousarray(t.to("cpu", torch.float64).numpy())
+    pool = f64(sb.pools[l][torch.tensor(used, dtype=torch.long, device=sb.device)]) if used else \
+        np.zeros((1, sb.HV, sb.V, sb.K))
+    return dict(q=f64(sb.q[l][idx]), k=f64(sb.k[l][idx]), v=f64(sb.v[l][idx]),
+                a=f64(sb.a[l][idx]), b=f64(sb.b[l][idx]), A_log=f64(sb.A_log[l]),
+                dt_bias=f64(sb.dt_bias[l]), token_start=new_start.numpy(), window_len=win.numpy(),
+                pool=pool, slot_table=new_table.numpy(),
+                seq_pos=None if sb.seq_pos is None else sb.seq_pos[rows].cpu().numpy(),
+                accepted_len=sb.accepted_len[rows].cpu().numpy())
+
+
+def _oracle_unit_of_work(oracle, d, sb):
+    v = oracle.spec_verify(q=d["q"], k=d["k"], v=d["v"], a=d["a"], b=d["b"], A_log=d["A_log"],
+                           dt_bias=d["dt_bias"], token_start=d["token_start"],
+                           window_len=d["window_len"], pool=d["pool"],
+                           slot_table=d["slot_table"], seq_pos=d["seq_pos"],
+                           block_size=sb.block_size, max_window=sb.W)
+    oracle.replay_commit(pools=d["pool"][None], rec_u=v["rec_u"][None], rec_k=v["rec_k"][None],
+                         rec_g=v["rec_g"][None], window_len=d["window_len"],
+                         accepted_len=d["accepted_len"], slot_table=d["slot_table"],
+                         seq_pos=d["seq_pos"], block_size=sb.block_size, max_window=sb.W)
+
+
+def cpu_baseline(sb, seconds):
+    """The fp64 oracle as it stands, on the host cores, over whole layers of
+    the same workload until the time budget is spent; scaled to a full step."""
+    import oracle
+    oracle.build()
+    rows = list(range(sb.B))
+    layers_done, spent = 0, 0.0
+    for l in range(sb.L):
+        d = _compact_layer(sb, l, rows)
+        t0 = time.perf_counter()
+        _oracle_unit_of_work(oracle, d, sb)
+        spent += time.perf_counter() - t0
+        layers_done += 1
+        if spent >= seconds:
+            break
+    us = spent / layers_done * sb.L * 1e6
+    return {"value": round(us, 1), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{layers_done} of {sb.L} layers (all {sb.B} rows), verify + commit, "
+                      f"{spent:.1f} s of CPU wall time, scaled to {sb.L} layers"}
+
+
+# ------------------------------------------------------ reference arm
+def run_reference(args, rank, world_size):
+    """The oracle on this workload, timed on the host cores: every step is a
+    bounded sample (a few rows of one layer), scaled to the full step."""
+    import oracle
+    oracle.build()
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    sd = torch.bfloat16 if args.state_dtype == "bf16" else torch.float32
+    sb = make_workload(args.workload, dev, 0, sd)
+    live = [r for r in range(sb.B) if int(sb.window_len[r]) > 0 and int(sb.slot_table[r, 0]) >= 0] \
+        if sb.block_size == 0 else list(range(sb.B))
+    n_steps = args.warmup + args.steps
+    budget = max(0.02, min(1.0, 150.0 / n_steps))
+    # size the per-step row sample against the budget
+    d1 = _compact_layer(sb, 0, live[:1])
+    t0 = time.perf_counter()
+    _oracle_unit_of_work(oracle, d1, sb)
+    per_row = max(time.perf_counter() - t0, 1e-4)
+    nrows = max(1, min(len(live), int(budget / per_row)))
+    samples = []
+    for i in range(n_steps):
+        l = i % sb.L
+        rows = [live[(i * nrows + j) % len(live)] for j in range(nrows)]
+        d = _compact_layer(sb, l, rows)
+        t0 = time.perf_counter()
+        _oracle_unit_of_work(oracle, d, sb)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            samples.append(dt)
+    per_step = statistics.mean(samples) * (len(live) / nrows) * sb.L
+    us = per_step * 1e6
+    sample = (f"each step: {nrows} of {len(live)} live rows of one layer (verify + commit), "
+              f"scaled to {len(live)} rows x {sb.L} layers")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
+        "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; see workloads.py)",
+        "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
+                   "state_dtype": args.state_dtype},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, local_rank, world_size = dist.world()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world_size)), flush=True)
+        return 0
+    rank, local_rank, world_size = dist.init("nccl")
+    try:
+        result = run_gpu(args, rank, local_rank, world_size)
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+    finally:
+        dist.finalize()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

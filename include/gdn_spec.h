@@ -1,0 +1,192 @@
+/*
+ * gdn_spec.h -- C ABI of libgdn_spec.so: speculative (MTP) verify and
+ * all-layer replay commit for Gated DeltaNet (GDN) layers on one GPU.
+ *
+ * The method (vLLM PR "[Spec Decode][Qwen4Exp] RecoverSSM for Qwen GDN and
+ * the PLE short conv", Purpose; tokenspeed PR "feat: add Qwen3.5 GDN
+ * ReplaySSM", Summary and Motivation):
+ *   - the verify runs each request's draft window from a read-only
+ *     checkpoint state, writes the per-token outputs and a small per-token
+ *     replay record [correction u (V), normalized key (K), gate (1)] in
+ *     fp32, and writes no state;
+ *   - after sampling, one commit launch over all layers replays only the
+ *     accepted prefix, h = fma(u, k, h * decay), and writes each state once
+ *     (plus the block-boundary state in align mode);
+ *   - the native baseline instead stores the full state after every draft
+ *     position.
+ *
+ * Recurrence, per value head h with a [V][K] fp32 state S (K contiguous):
+ *   alpha_t = exp(-exp(A_log[h]) * softplus(a[t,h] + dt_bias[h]))
+ *   beta_t  = sigmoid(b[t,h])
+ *   khat_t  = k_t / sqrt(|k_t|^2 + 1e-6),  qhat_t likewise
+ *   H = alpha_t * S;  u_t = beta_t * (v_t - H khat_t);  S = H + u_t khat_t^T
+ *   o_t = S qhat_t
+ * Value head h reads key head h / (num_v_heads / num_k_heads).
+ * All three kernels run the same fp32 operations in the same order, so the
+ * verify's outputs equal the native kernel's and a commit after n accepted
+ * tokens equals the native state after token n, bit for bit.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer is device memory owned by the caller, except `shape`,
+ *     which is a host pointer read during the call only.  The library never
+ *     allocates, frees or synchronises; it enqueues kernels on `stream`
+ *     (a cudaStream_t; NULL = legacy default stream) on the current device
+ *     and returns.
+ *   - Return value: GDN_OK, or a negative GDN_ERR_* for a problem the host
+ *     can see (null pointer, unsupported shape, bad stride or alignment,
+ *     failed launch).  Nothing is launched when the return is negative.
+ *   - Row-level problems are found on the device: the row is skipped (it
+ *     writes nothing) and its GDN_ROW_ERR_* bits are OR-ed into *err when
+ *     err is not NULL.  The caller clears *err beforehand.
+ *   - Null rows: a row whose window_len is 0 or whose checkpoint slot is -1
+ *     reads and writes nothing (graph padding rows; vLLM PR above, Purpose).
+ *   - Slot of the state after x folded tokens of row r:
+ *       block_size == 0: slot_table[r * slot_table_stride + 0]
+ *       block_size  > 0: slot_table[r * slot_table_stride + (x - 1) / block_size]
+ *     (align mode: a state lives in the block of its last token; vLLM PR
+ *     above, Commits item 3).  The checkpoint is the state after
+ *     x = seq_pos[r] tokens; seq_pos is read only in align mode.
+ *
+ * Supported shapes: head_k, head_v in {16, 32, 64, 128}; max_window 1..16;
+ * num_v_heads a multiple of num_k_heads; batch, num_layers <= 65535.
+ */
+#ifndef GDN_SPEC_H_
+#define GDN_SPEC_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+#define GDN_DTYPE_F32 0
+#define GDN_DTYPE_BF16 1
+
+/* Return codes. */
+#define GDN_OK 0
+#define GDN_ERR_NULL (-1)        /* a required pointer is NULL                */
+#define GDN_ERR_UNSUPPORTED (-2) /* shape or dtype outside the supported set  */
+#define GDN_ERR_INVALID (-3)     /* bad count, stride, alignment or block size */
+#define GDN_ERR_CUDA (-4)        /* the kernel launch failed                   */
+
+/* Row error bits OR-ed into *err. */
+#define GDN_ROW_ERR_WINDOW 1     /* window_len outside [0, max_window]                */
+#define GDN_ROW_ERR_ACCEPTED 2   /* accepted_len outside [0, window_len]              */
+#define GDN_ROW_ERR_SLOT 4       /* slot outside [-1, num_slots)                      */
+#define GDN_ROW_ERR_BLOCK 8      /* align mode: a needed column is outside the table, */
+                                 /* or holds -1 although the row is live             */
+#define GDN_ROW_ERR_SEQPOS 16    /* align mode: seq_pos < 1 on a live row             */
+#define GDN_ROW_ERR_TOKENS 32    /* token rows outside [0, num_tokens)                */
+
+typedef struct gdn_shape {
+  int32_t num_k_heads; /* HK                                              */
+  int32_t num_v_heads; /* HV, a multiple of HK                            */
+  int32_t head_k;      /* K: key width, the state's contiguous dimension   */
+  int32_t head_v;      /* V: value width, the state's row count            */
+  int32_t max_window;  /* W: record stride in tokens, 1..16                */
+  int32_t qkv_dtype;   /* GDN_DTYPE_F32 or GDN_DTYPE_BF16 for q, k, v      */
+  int32_t state_dtype; /* GDN_DTYPE_F32 or GDN_DTYPE_BF16 for the state    */
+} gdn_shape;
+
+/*
+ * Speculative verify of one layer (vLLM PR above, Purpose and Commits
+ * item 2: the verify reads strided q/k/v views of the conv output and
+ * writes straight into the layer output).
+ *
+ *   q, k          [num_tokens][HK][K] of qkv_dtype; token row t starts at
+ *                 q + t * q_row_stride (elements), heads contiguous inside a
+ *                 row.  Base 16-byte aligned (fp32) or 8-byte (bf16); row
+ *                 stride a multiple of 4 elements.
+ *   v             [num_tokens][HV][V] of qkv_dtype, row stride v_row_stride.
+ *   a, b          [num_tokens][HV] fp32, contiguous: raw gate inputs.
+ *   A_log, dt_bias [HV] fp32.
+ *   token_start, window_len [batch] int32: row r owns token rows
+ *                 token_start[r] .. token_start[r] + window_len[r] - 1.
+ *                 Rows need not be contiguous or ordered.
+ *   state_pool    [num_slots][HV][V][K] of state_dtype, 16-byte aligned.
+ *                 Read only: the checkpoint is never written.
+ *   slot_table    [batch][slot_table_stride] int32; seq_pos [batch] int32
+ *                 (align mode only, else may be NULL); block_size >= 0.
+ *   out           [num_tokens][HV][V] fp32, row stride out_row_stride:
+ *                 o_t for every token of every live row; other rows are not
+ *                 touched.
+ *   rec_u [batch][HV][W][V], rec_k [batch][HV][W][K], rec_g [batch][HV][W]
+ *                 fp32, 16-byte aligned: the replay record of token t of row
+ *                 r in position t; positions >= window_len[r] are untouched.
+ *   err           optional int32 row-error word.
+ */
+int gdn_spec_verify(const gdn_shape* shape, int32_t batch, int32_t num_tokens,
+                    int32_t num_slots, const void* q, int64_t q_row_stride,
+                    const void* k, int64_t k_row_stride, const void* v,
+                    int64_t v_row_stride, const float* a, const float* b,
+                    const float* A_log, const float* dt_bias,
+                    const int32_t* token_start, const int32_t* window_len,
+                    const void* state_pool, const int32_t* slot_table,
+                    int32_t slot_table_stride, const int32_t* seq_pos,
+                    int32_t block_size, float* out, int64_t out_row_stride,
+                    float* rec_u, float* rec_k, float* rec_g, int32_t* err,
+                    void* stream);
+
+/*
+ * All-layer replay commit in one launch (tokenspeed PR above, Summary and
+ * Implementation: layer-indexed state pools and replay buffers, a single
+ * replay kernel over all GDN layers; vLLM PR above, Purpose and Commits
+ * items 3 and 6).
+ *
+ *   state_pools   device array of num_layers device pointers, each to a
+ *                 [num_slots][HV][V][K] pool of state_dtype (16-byte
+ *                 aligned), updated in place.
+ *   rec_u, rec_k, rec_g  device arrays of num_layers device pointers to the
+ *                 layer's records, laid out as gdn_spec_verify writes them.
+ *   window_len, accepted_len [batch] int32; slot_table, seq_pos, block_size
+ *                 as for gdn_spec_verify (the same values the verify saw).
+ * For each live row with n = accepted_len[r] > 0 the state after n tokens
+ * is written to slot(seq_pos + n) (slot(n) without align mode, i.e. in
+ * place).  In align mode each block boundary p with seq_pos < p <
+ * seq_pos + n, p % block_size == 0, also receives the state after
+ * p - seq_pos tokens in slot(p); a boundary at seq_pos + n is the final
+ * state and is written once.  Every write starts from the unmodified
+ * checkpoint, so a boundary slot equal to the checkpoint slot is safe
+ * (final folds before boundary folds).  A bf16 state is rounded once per
+ * stored state (round to nearest even).  Rows with n == 0 or a null slot
+ * write nothing.
+ */
+int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers,
+                      int32_t batch, int32_t num_slots,
+                      void* const* state_pools, const float* const* rec_u,
+                      const float* const* rec_k, const float* const* rec_g,
+                      const int32_t* window_len, const int32_t* accepted_len,
+                      const int32_t* slot_table, int32_t slot_table_stride,
+                      const int32_t* seq_pos, int32_t block_size, int32_t* err,
+                      void* stream);
+
+/*
+ * Native baseline of one layer: the verify's recurrence with the full
+ * state stored after every draft position, and no record (vLLM PR above,
+ * Purpose: the path that snapshots the recurrent state after every draft
+ * position; tokenspeed PR above, Motivation).
+ *
+ * Arguments as gdn_spec_verify up to out_row_stride, then
+ *   snapshots     [batch][W][HV][V][K] of state_dtype, 16-byte aligned:
+ *                 snapshots[r][t] = state after token t of row r
+ *                 (t < window_len[r]); a bf16 state is rounded once per
+ *                 stored snapshot.  Other positions are untouched and the
+ *                 checkpoint pool is never written.
+ */
+int gdn_native_spec_snapshot(
+    const gdn_shape* shape, int32_t batch, int32_t num_tokens,
+    int32_t num_slots, const void* q, int64_t q_row_stride, const void* k,
+    int64_t k_row_stride, const void* v, int64_t v_row_stride, const float* a,
+    const float* b, const float* A_log, const float* dt_bias,
+    const int32_t* token_start, const int32_t* window_len,
+    const void* state_pool, const int32_t* slot_table,
+    int32_t slot_table_stride, const int32_t* seq_pos, int32_t block_size,
+    float* out, int64_t out_row_stride, void* snapshots, int32_t* err,
+    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_SPEC_H_ */

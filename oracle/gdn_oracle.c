@@ -163,12 +163,13 @@ void gdn_oracle_replay(int K, int V, int n, double* S, const double* u,
  * Without align mode (block_size == 0) a request owns one slot, column 0.
  * In align mode the state after x tokens lives in the block of its last
  * token, column (x - 1) / block_size (vLLM PR above, Commits item 3).
- * Returns -2 if the column lies outside the table. */
+ * Returns OUTSIDE_TABLE if the column lies outside the table. */
+#define OUTSIDE_TABLE INT32_MIN
 static int32_t slot_after(const int32_t* table_row, int table_stride,
                           int block_size, long x) {
   if (block_size == 0) return table_row[0];
   long col = (x - 1) / block_size;
-  if (x < 1 || col >= table_stride) return -2;
+  if (x < 1 || col >= table_stride) return OUTSIDE_TABLE;
   return table_row[col];
 }
 
@@ -183,7 +184,7 @@ int gdn_oracle_source_slot(int window_len, const int32_t* table_row,
   if (window_len == 0) return -1;
   if (block_size > 0 && seq_pos < 1) return -(1 + ORACLE_ERR_SEQPOS);
   int32_t s = slot_after(table_row, table_stride, block_size, seq_pos);
-  if (s == -2) return -(1 + ORACLE_ERR_BLOCK);
+  if (s == OUTSIDE_TABLE) return -(1 + ORACLE_ERR_BLOCK);
   if (s < -1 || s >= num_slots) return -(1 + ORACLE_ERR_SLOT);
   return s;
 }
@@ -214,7 +215,7 @@ int gdn_oracle_commit_plan(int window_len, int accepted_len,
   int n = accepted_len;
   int nw = 0;
   int32_t fin = slot_after(table_row, table_stride, block_size, p0 + n);
-  if (fin == -2 || fin == -1) return -(1 + ORACLE_ERR_BLOCK);
+  if (fin == OUTSIDE_TABLE || fin == -1) return -(1 + ORACLE_ERR_BLOCK);
   if (fin < -1 || fin >= num_slots) return -(1 + ORACLE_ERR_SLOT);
   if (nw < max_writes) { out_slot[nw] = fin; out_ntok[nw] = n; }
   ++nw;
@@ -222,7 +223,7 @@ int gdn_oracle_commit_plan(int window_len, int accepted_len,
     for (long p = p0 + 1; p < p0 + n; ++p) {
       if (p % block_size != 0) continue;
       int32_t s = slot_after(table_row, table_stride, block_size, p);
-      if (s == -2 || s == -1) return -(1 + ORACLE_ERR_BLOCK);
+      if (s == OUTSIDE_TABLE || s == -1) return -(1 + ORACLE_ERR_BLOCK);
       if (s < -1 || s >= num_slots) return -(1 + ORACLE_ERR_SLOT);
       if (nw < max_writes) { out_slot[nw] = s; out_ntok[nw] = (int32_t)(p - p0); }
       ++nw;

@@ -1,0 +1,233 @@
+"""Thin Python binding of libgdn_spec.so: argument marshalling only.
+
+Each function takes torch CUDA tensors, checks that their layout is the one
+the C ABI documents (include/gdn_spec.h), and passes raw device pointers,
+sizes and the current CUDA stream to the library function of the same
+name.  Every step of the computation runs in the library's kernels; there
+is no fallback.  A missing library raises at the first call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
+ROW_ERR_WINDOW, ROW_ERR_ACCEPTED, ROW_ERR_SLOT = 1, 2, 4
+ROW_ERR_BLOCK, ROW_ERR_SEQPOS, ROW_ERR_TOKENS = 8, 16, 32
+ENTRY_POINTS = ("gdn_spec_verify", "gdn_replay_commit", "gdn_native_spec_snapshot")
+
+_ERRORS = {-1: "null pointer", -2: "unsupported shape or dtype",
+           -3: "invalid count, stride, alignment or block size", -4: "CUDA launch failed"}
+
+
+class GDNError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code} ({_ERRORS.get(code, 'unknown')})")
+        self.code = code
+
+
+class gdn_shape(ctypes.Structure):
+    _fields_ = [("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
+                ("head_k", ctypes.c_int32), ("head_v", ctypes.c_int32),
+                ("max_window", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32),
+                ("state_dtype", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+_P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+_VERIFY_HEAD = [ctypes.POINTER(gdn_shape), _I32, _I32, _I32, _P, _I64, _P, _I64, _P, _I64,
+                _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _P, _I64]
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libgdn_spec.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with spec_decode_recurrent_gb300.build.build()")
+            lib = ctypes.CDLL(path)
+            lib.gdn_spec_verify.restype = ctypes.c_int
+            lib.gdn_spec_verify.argtypes = _VERIFY_HEAD + [_P, _P, _P, _P, _P]
+            lib.gdn_native_spec_snapshot.restype = ctypes.c_int
+            lib.gdn_native_spec_snapshot.argtypes = _VERIFY_HEAD + [_P, _P, _P]
+            lib.gdn_replay_commit.restype = ctypes.c_int
+            lib.gdn_replay_commit.argtypes = [ctypes.POINTER(gdn_shape), _I32, _I32, _I32,
+                                              _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32,
+                                              _P, _P]
+            _lib = lib
+    return _lib
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return GDN_DTYPE_F32
+    if t == torch.bfloat16:
+        return GDN_DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _rows(t: torch.Tensor, name: str, dtype=None):
+    """[rows, heads, width] view with contiguous heads; returns the row stride."""
+    _need(t.dim() == 3 and t.is_cuda, f"{name} must be a 3-d CUDA tensor")
+    _need(t.stride(2) == 1 and t.stride(1) == t.shape[2], f"{name}: heads must be contiguous")
+    if dtype is not None:
+        _need(t.dtype == dtype, f"{name} must be {dtype}")
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1] * t.shape[2]
+
+
+def _contig(t: torch.Tensor, name: str, dtype):
+    _need(t.is_cuda and t.is_contiguous() and t.dtype == dtype,
+          f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def _verify_args(q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+                 slot_table, seq_pos, block_size, out, max_window):
+    T, HK, K = q.shape
+    _need(k.shape == q.shape and k.dtype == q.dtype, "k must match q")
+    _need(v.shape[0] == T and v.dtype == q.dtype, "v must have q's rows and dtype")
+    HV, V = v.shape[1], v.shape[2]
+    qs, ks, vs = _rows(q, "q"), _rows(k, "k"), _rows(v, "v")
+    os_ = _rows(out, "out", torch.float32)
+    _need(out.shape == (T, HV, V), "out must be [num_tokens, HV, V]")
+    _need(state_pool.dim() == 4 and state_pool.shape[1:] == (HV, V, K), "pool must be [slots, HV, V, K]")
+    _contig(state_pool, "state_pool", state_pool.dtype)
+    for name, t, n in (("a", a, None), ("b", b, None)):
+        _contig(t, name, torch.float32)
+        _need(t.shape == (T, HV), f"{name} must be [num_tokens, HV]")
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias)):
+        _contig(t, name, torch.float32)
+        _need(t.numel() == HV, f"{name} must have HV entries")
+    B = window_len.shape[0]
+    for name, t in (("token_start", token_start), ("window_len", window_len)):
+        _contig(t, name, torch.int32)
+        _need(t.shape == (B,), f"{name} must be [batch]")
+    st = slot_table if slot_table.dim() == 2 else slot_table.view(-1, 1)
+    _contig(st, "slot_table", torch.int32)
+    _need(st.shape[0] == B, "slot_table must have one row per request")
+    if block_size:
+        _contig(seq_pos, "seq_pos", torch.int32)
+    shape = gdn_shape(HK, HV, K, V, int(max_window), _dtype_code(q.dtype),
+                      _dtype_code(state_pool.dtype))
+    head = [ctypes.byref(shape), B, T, state_pool.shape[0], _ptr(q), qs, _ptr(k), ks, _ptr(v), vs,
+            _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(token_start), _ptr(window_len),
+            _ptr(state_pool), _ptr(st), st.shape[1], _ptr(seq_pos if block_size else None),
+            int(block_size), _ptr(out), os_]
+    return shape, head, B, HV, V, K
+
+
+def gdn_spec_verify(*, q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+                    slot_table, out, rec_u, rec_k, rec_g, max_window, seq_pos=None,
+                    block_size=0, err=None, stream=None) -> None:
+    """Verify one layer: writes out and the replay record, never the pool."""
+    shape, head, B, HV, V, K = _verify_args(q, k, v, a, b, A_log, dt_bias, token_start,
+                                            window_len, state_pool, slot_table, seq_pos,
+                                            block_size, out, max_window)
+    W = int(max_window)
+    for name, t, shp in (("rec_u", rec_u, (B, HV, W, V)), ("rec_k", rec_k, (B, HV, W, K)),
+                         ("rec_g", rec_g, (B, HV, W))):
+        _contig(t, name, torch.float32)
+        _need(tuple(t.shape) == shp, f"{name} must be {shp}")
+    if err is not None:
+        _contig(err, "err", torch.int32)
+    rc = load().gdn_spec_verify(*head, _ptr(rec_u), _ptr(rec_k), _ptr(rec_g), _ptr(err),
+                                _stream(stream))
+    if rc != 0:
+        raise GDNError("gdn_spec_verify", rc)
+
+
+def gdn_native_spec_snapshot(*, q, k, v, a, b, A_log, dt_bias, token_start, window_len,
+                             state_pool, slot_table, out, snapshots, max_window, seq_pos=None,
+                             block_size=0, err=None, stream=None) -> None:
+    """Native baseline of one layer: writes out and the state after every token."""
+    shape, head, B, HV, V, K = _verify_args(q, k, v, a, b, A_log, dt_bias, token_start,
+                                            window_len, state_pool, slot_table, seq_pos,
+                                            block_size, out, max_window)
+    W = int(max_window)
+    _contig(snapshots, "snapshots", state_pool.dtype)
+    _need(tuple(snapshots.shape) == (B, W, HV, V, K), "snapshots must be [batch, W, HV, V, K]")
+    if err is not None:
+        _contig(err, "err", torch.int32)
+    rc = load().gdn_native_spec_snapshot(*head, _ptr(snapshots), _ptr(err), _stream(stream))
+    if rc != 0:
+        raise GDNError("gdn_native_spec_snapshot", rc)
+
+
+class LayerTable:
+    """Device arrays of per-layer pointers (pools and records) for the
+    all-layer commit.  Build once per set of buffers and reuse."""
+
+    def __init__(self, pools: Sequence[torch.Tensor], rec_u: Sequence[torch.Tensor],
+                 rec_k: Sequence[torch.Tensor], rec_g: Sequence[torch.Tensor]):
+        L = len(pools)
+        _need(L >= 1 and len(rec_u) == len(rec_k) == len(rec_g) == L, "one entry per layer")
+        p0 = pools[0]
+        for t in pools:
+            _contig(t, "pool", p0.dtype)
+            _need(t.shape == p0.shape and t.device == p0.device, "pools must share shape")
+        for name, lst in (("rec_u", rec_u), ("rec_k", rec_k), ("rec_g", rec_g)):
+            for t in lst:
+                _contig(t, name, torch.float32)
+        dev = p0.device
+        mk = lambda ts: torch.tensor([t.data_ptr() for t in ts], dtype=torch.int64, device=dev)
+        self.pools, self.rec_u, self.rec_k, self.rec_g = list(pools), list(rec_u), list(rec_k), list(rec_g)
+        self.d_pools, self.d_rec_u, self.d_rec_k, self.d_rec_g = mk(pools), mk(rec_u), mk(rec_k), mk(rec_g)
+        self.num_layers = L
+        self.num_slots, self.HV, self.V, self.K = p0.shape
+        self.state_dtype = p0.dtype
+        self.B, _, self.W, _ = rec_u[0].shape
+
+
+def gdn_replay_commit(*, table: LayerTable, num_k_heads: int, window_len, accepted_len,
+                      slot_table, seq_pos=None, block_size=0, err=None, stream=None) -> None:
+    """All-layer commit in one launch: replays the accepted prefix of every
+    row of every layer and writes each state once (plus align boundaries)."""
+    B = window_len.shape[0]
+    _need(B == table.B, "batch must match the record buffers")
+    for name, t in (("window_len", window_len), ("accepted_len", accepted_len)):
+        _contig(t, name, torch.int32)
+        _need(t.shape == (B,), f"{name} must be [batch]")
+    st = slot_table if slot_table.dim() == 2 else slot_table.view(-1, 1)
+    _contig(st, "slot_table", torch.int32)
+    if block_size:
+        _contig(seq_pos, "seq_pos", torch.int32)
+    if err is not None:
+        _contig(err, "err", torch.int32)
+    # the commit reads no q/k/v: qkv_dtype is a placeholder
+    shape = gdn_shape(int(num_k_heads), table.HV, table.K, table.V, table.W, GDN_DTYPE_F32,
+                      _dtype_code(table.state_dtype))
+    rc = load().gdn_replay_commit(
+        ctypes.byref(shape), table.num_layers, B, table.num_slots, _ptr(table.d_pools),
+        _ptr(table.d_rec_u), _ptr(table.d_rec_k), _ptr(table.d_rec_g), _ptr(window_len),
+        _ptr(accepted_len), _ptr(st), st.shape[1], _ptr(seq_pos if block_size else None),
+        int(block_size), _ptr(err), _stream(stream))
+    if rc != 0:
+        raise GDNError("gdn_replay_commit", rc)

@@ -1,0 +1,187 @@
+// gdn_device.cuh -- device helpers shared by the verify, native-snapshot and
+// commit kernels of libgdn_spec.so.
+//
+// Every floating-point step of the recurrence is written with explicit
+// round-to-nearest intrinsics (__fmul_rn, __fmaf_rn, ...) and the library is
+// compiled with -fmad=false, so no kernel can contract a multiply and an add
+// differently from another.  That is what makes the verify's outputs equal
+// to the native kernel's, and a commit after n accepted tokens equal to the
+// native state after token n, bit for bit (vLLM PR "[Spec Decode][Qwen4Exp]
+// RecoverSSM for Qwen GDN and the PLE short conv", Test Result: the commit
+// replays forward with the same update h = fma(c, k, h * decay)).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <limits.h>
+#include <stdint.h>
+
+#include "gdn_spec.h"
+
+namespace gdn {
+
+constexpr int kMaxWindow = 16;
+constexpr float kL2NormEps = 1e-6f;
+
+// ------------------------------------------------------------ parameters
+struct VerifyParams {
+  int HK, HV, V, W;
+  int batch, num_tokens, num_slots;
+  const void* q;
+  const void* k;
+  const void* v;
+  long long q_stride, k_stride, v_stride;  // elements per token row
+  const float* a;
+  const float* b;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* token_start;
+  const int32_t* window_len;
+  const void* pool;
+  const int32_t* slot_table;
+  int table_stride;
+  const int32_t* seq_pos;
+  int block_size;
+  float* out;
+  long long out_stride;
+  float* rec_u;
+  float* rec_k;
+  float* rec_g;
+  void* snaps;
+  int32_t* err;
+};
+
+struct CommitParams {
+  int HV, V, W;
+  int num_layers, batch, num_slots;
+  void* const* pools;
+  const float* const* rec_u;
+  const float* const* rec_k;
+  const float* const* rec_g;
+  const int32_t* window_len;
+  const int32_t* accepted_len;
+  const int32_t* slot_table;
+  int table_stride;
+  const int32_t* seq_pos;
+  int block_size;
+  int32_t* err;
+};
+
+// ----------------------------------------------------------------- gates
+// softplus(x) = log(1 + e^x), in the form that does not overflow.
+__device__ __forceinline__ float softplus(float x) {
+  return x > 0.0f ? __fadd_rn(x, log1pf(expf(-x))) : log1pf(expf(x));
+}
+
+// Decay alpha = exp(g), g = -exp(A_log) * softplus(a + dt_bias).
+__device__ __forceinline__ float gate_decay(float a, float A_log, float dt_bias) {
+  float g = -__fmul_rn(expf(A_log), softplus(__fadd_rn(a, dt_bias)));
+  return expf(g);
+}
+
+// Write strength beta = sigmoid(b).
+__device__ __forceinline__ float gate_beta(float b) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-b)));
+}
+
+// ------------------------------------------------------ element loads
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// Four consecutive elements starting at p (16-byte aligned for fp32,
+// 8-byte aligned for bf16), widened exactly to fp32.
+__device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
+  float4 t = *reinterpret_cast<const float4*>(p);
+  x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
+  uint2 t = *reinterpret_cast<const uint2*>(p);
+  x[0] = bf16_bits_to_float(t.x & 0xffffu);
+  x[1] = bf16_bits_to_float(t.x >> 16);
+  x[2] = bf16_bits_to_float(t.y & 0xffffu);
+  x[3] = bf16_bits_to_float(t.y >> 16);
+}
+__device__ __forceinline__ float load1(const float* p) { return *p; }
+__device__ __forceinline__ float load1(const __nv_bfloat16* p) {
+  return bf16_bits_to_float(*reinterpret_cast<const unsigned short*>(p));
+}
+
+// State loads bypass L1 (ld.global.cg): a state tile is read once.
+__device__ __forceinline__ void load_state4(const float* p, float (&x)[4]) {
+  float4 t = __ldcg(reinterpret_cast<const float4*>(p));
+  x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+}
+__device__ __forceinline__ void load_state4(const __nv_bfloat16* p, float (&x)[4]) {
+  uint2 t = __ldcg(reinterpret_cast<const uint2*>(p));
+  x[0] = bf16_bits_to_float(t.x & 0xffffu);
+  x[1] = bf16_bits_to_float(t.x >> 16);
+  x[2] = bf16_bits_to_float(t.y & 0xffffu);
+  x[3] = bf16_bits_to_float(t.y >> 16);
+}
+
+// Round-to-nearest-even to bf16, the single rounding of a stored state.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return a | (b << 16);
+}
+
+__device__ __forceinline__ void store_state4(float* p, const float (&x)[4]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
+}
+__device__ __forceinline__ void store_state4(__nv_bfloat16* p, const float (&x)[4]) {
+  uint2 t;
+  t.x = pack_bf16x2(x[0], x[1]);
+  t.y = pack_bf16x2(x[2], x[3]);
+  __stcs(reinterpret_cast<uint2*>(p), t);
+}
+
+// --------------------------------------------------------- the recurrence
+// One element's decay-then-write, the commit's fold and the verify's state
+// update: S = fma(u, khat, S * alpha).
+__device__ __forceinline__ float fold(float s, float alpha, float u, float kh) {
+  return __fmaf_rn(u, kh, __fmul_rn(s, alpha));
+}
+
+// ----------------------------------------------------------- row planning
+// Row plan shared by the kernels: checks a row against the documented
+// contract, in the same order the error bits are documented.
+struct SourceSlot {
+  int slot;  // >= 0 live, -1 null row
+  int err;   // GDN_ROW_ERR_* bits, 0 if fine
+};
+
+constexpr int kOutsideTable = INT_MIN;
+
+// Slot holding the state after x folded tokens (block_size == 0: column 0).
+// Returns kOutsideTable when the column lies outside the table.
+__device__ __forceinline__ int slot_after(const int32_t* row, int stride,
+                                          int block_size, long long x) {
+  if (block_size == 0) return row[0];
+  if (x < 1) return kOutsideTable;
+  long long col = (x - 1) / block_size;
+  if (col >= stride) return kOutsideTable;
+  return row[col];
+}
+
+__device__ __forceinline__ SourceSlot source_slot(int w, int W, const int32_t* row,
+                                                  int stride, int block_size,
+                                                  const int32_t* seq_pos, int r,
+                                                  int num_slots) {
+  SourceSlot s{-1, 0};
+  if (w < 0 || w > W) { s.err = GDN_ROW_ERR_WINDOW; return s; }
+  if (w == 0) return s;
+  long long p0 = 0;
+  if (block_size > 0) {
+    p0 = seq_pos[r];
+    if (p0 < 1) { s.err = GDN_ROW_ERR_SEQPOS; return s; }
+  }
+  int slot = slot_after(row, stride, block_size, p0);
+  if (slot == kOutsideTable) { s.err = GDN_ROW_ERR_BLOCK; return s; }
+  if (slot < -1 || slot >= num_slots) { s.err = GDN_ROW_ERR_SLOT; return s; }
+  s.slot = slot;
+  return s;
+}
+
+}  // namespace gdn

@@ -1,0 +1,288 @@
+// gdn_verify.cu -- speculative verify and native per-draft snapshot kernels.
+//
+// One CTA of 4 warps owns a tile of VT state rows of one (request row,
+// value head) and runs the whole draft window over it with the tile held in
+// registers (tokenspeed PR "feat: add Qwen3.5 GDN ReplaySSM", Summary and
+// Implementation: a cooperative 4-warp CTA per 128x128 state head; here the
+// head is additionally split into V tiles so that small batches still fill
+// 152 SMs).  Rows of S are independent given (khat, qhat, alpha, beta, v_i),
+// so tiles never communicate; the only reductions are over K, inside a
+// group of K/16 lanes, by warp shuffles.
+//
+// Register layout of a tile, for K = 128: LPR = 8 lanes share one state row
+// and each lane holds 16 of its columns, as four 4-column chunks at columns
+// 4 * (l + LPR * m), m = 0..3, so a warp's load of chunk m reads whole
+// 128-byte lines.  A warp covers RPW = 32 / LPR rows per row group and each
+// thread keeps RPT row groups.
+//
+// VERIFY mode writes o_t and the replay record (u_t, khat_t, alpha_t) and no
+// state (vLLM PR "[Spec Decode][Qwen4Exp] RecoverSSM for Qwen GDN and the
+// PLE short conv", Purpose).  NATIVE mode writes o_t and the full state after
+// every token instead.  Both run the identical arithmetic, so their outputs
+// agree bit for bit.
+#include "gdn_device.cuh"
+#include "gdn_launch.h"
+
+namespace gdn {
+
+template <int K>
+struct VerifyTile {
+  static constexpr int LPR = K / 16;          // lanes per state row
+  static constexpr int RPW = 32 / LPR;        // rows per warp per row group
+  static constexpr int RPT = (K == 128) ? 2 : 1;  // row groups per thread
+  static constexpr int WARPS = 4;
+  static constexpr int THREADS = 32 * WARPS;
+  static constexpr int VT = WARPS * RPW * RPT;    // state rows per CTA
+  static constexpr int CPL = 16;              // columns per lane
+};
+
+// Dynamic shared memory of one verify CTA, in floats.
+template <int K>
+__host__ __device__ constexpr int verify_smem_floats(int W) {
+  return W * (2 * K + VerifyTile<K>::VT + 2);
+}
+
+template <int K, typename QKV, typename ST, bool NATIVE>
+__global__ void __launch_bounds__(VerifyTile<K>::THREADS)
+    gdn_verify_kernel(const VerifyParams p) {
+  using Tile = VerifyTile<K>;
+  constexpr int LPR = Tile::LPR, RPW = Tile::RPW, RPT = Tile::RPT, VT = Tile::VT;
+  extern __shared__ float smem[];
+
+  const int ntiles = (p.V + VT - 1) / VT;
+  const int tile = blockIdx.x % ntiles;
+  const int h = blockIdx.x / ntiles;
+  const int r = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- row plan: identical checks in every CTA of the row
+  const int w = p.window_len[r];
+  const int32_t* trow = p.slot_table + (size_t)r * p.table_stride;
+  SourceSlot src = source_slot(w, p.W, trow, p.table_stride, p.block_size,
+                               p.seq_pos, r, p.num_slots);
+  long long t0 = 0;
+  if (!src.err && src.slot >= 0) {
+    t0 = p.token_start[r];
+    if (t0 < 0 || t0 + w > p.num_tokens) src.err = GDN_ROW_ERR_TOKENS;
+  }
+  if (src.err) {
+    if (p.err && tid == 0 && tile == 0 && h == 0) atomicOr(p.err, src.err);
+    return;
+  }
+  if (src.slot < 0) return;  // null row or empty window: writes nothing
+
+  const int group = p.HV / p.HK;
+  const int hk = h / group;
+  const int l = lane % LPR;   // column lane inside the row group
+  const int lr = lane / LPR;  // row inside the warp's row group
+
+  // ---- issue the checkpoint tile loads first; they stay in flight while
+  // ---- the token inputs are staged
+  const ST* S0 = static_cast<const ST*>(p.pool) +
+                 ((size_t)src.slot * p.HV + h) * (size_t)p.V * K;
+  float s[RPT][16];
+  int rows[RPT];
+#pragma unroll
+  for (int g = 0; g < RPT; ++g) {
+    rows[g] = tile * VT + (g * Tile::WARPS + warp) * RPW + lr;
+    if (rows[g] < p.V) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        float x[4];
+        load_state4(S0 + (size_t)rows[g] * K + 4 * (l + LPR * m), x);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[g][4 * m + e] = x[e];
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s[g][e] = 0.0f;
+    }
+  }
+
+  // ---- stage normalised keys / queries, values and gates in shared memory
+  float* kh_s = smem;                   // [W][K]
+  float* qh_s = kh_s + p.W * K;         // [W][K]
+  float* v_s = qh_s + p.W * K;          // [W][VT]
+  float* al_s = v_s + p.W * VT;         // [W]
+  float* be_s = al_s + p.W;             // [W]
+  const QKV* qb = static_cast<const QKV*>(p.q);
+  const QKV* kb = static_cast<const QKV*>(p.k);
+  const QKV* vb = static_cast<const QKV*>(p.v);
+  for (int t = warp; t < w; t += Tile::WARPS) {
+    const long long row_t = t0 + t;
+    float kx[4] = {0.f, 0.f, 0.f, 0.f}, qx[4] = {0.f, 0.f, 0.f, 0.f};
+    if (lane < K / 4) {
+      load4(kb + row_t * p.k_stride + (size_t)hk * K + 4 * lane, kx);
+      load4(qb + row_t * p.q_stride + (size_t)hk * K + 4 * lane, qx);
+    }
+    float ks = __fmul_rn(kx[0], kx[0]), qs = __fmul_rn(qx[0], qx[0]);
+#pragma unroll
+    for (int e = 1; e < 4; ++e) {
+      ks = __fmaf_rn(kx[e], kx[e], ks);
+      qs = __fmaf_rn(qx[e], qx[e], qs);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      ks = __fadd_rn(ks, __shfl_xor_sync(0xffffffffu, ks, off));
+      qs = __fadd_rn(qs, __shfl_xor_sync(0xffffffffu, qs, off));
+    }
+    const float kn = __fsqrt_rn(__fadd_rn(ks, kL2NormEps));
+    const float qn = __fsqrt_rn(__fadd_rn(qs, kL2NormEps));
+    if (lane < K / 4) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kh_s[t * K + 4 * lane + e] = __fdiv_rn(kx[e], kn);
+        qh_s[t * K + 4 * lane + e] = __fdiv_rn(qx[e], qn);
+      }
+    }
+    for (int i = lane; i < VT; i += 32) {
+      const int row = tile * VT + i;
+      v_s[t * VT + i] = row < p.V ? load1(vb + row_t * p.v_stride + (size_t)h * p.V + row) : 0.f;
+    }
+    if (lane == 0) {
+      const size_t gi = (size_t)row_t * p.HV + h;
+      al_s[t] = gate_decay(p.a[gi], p.A_log[h], p.dt_bias[h]);
+      be_s[t] = gate_beta(p.b[gi]);
+    }
+  }
+  __syncthreads();
+
+  const size_t rec_base = ((size_t)r * p.HV + h) * p.W;  // record position 0
+  if (!NATIVE && tile == 0) {
+    for (int i = tid; i < w * K; i += Tile::THREADS)
+      p.rec_k[rec_base * K + i] = kh_s[i];
+    if (tid < w) p.rec_g[rec_base + tid] = al_s[tid];
+  }
+
+  // ---- the draft window, token by token, state in registers
+  for (int t = 0; t < w; ++t) {
+    const float al = al_s[t], be = be_s[t];
+    float kk[16], qq[16];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float4 k4 = *reinterpret_cast<const float4*>(kh_s + t * K + 4 * (l + LPR * m));
+      const float4 q4 = *reinterpret_cast<const float4*>(qh_s + t * K + 4 * (l + LPR * m));
+      kk[4 * m + 0] = k4.x; kk[4 * m + 1] = k4.y; kk[4 * m + 2] = k4.z; kk[4 * m + 3] = k4.w;
+      qq[4 * m + 0] = q4.x; qq[4 * m + 1] = q4.y; qq[4 * m + 2] = q4.z; qq[4 * m + 3] = q4.w;
+    }
+    const long long orow = t0 + t;
+#pragma unroll
+    for (int g = 0; g < RPT; ++g) {
+      // H = alpha * S
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s[g][e] = __fmul_rn(s[g][e], al);
+      // d = H khat: four chunk partials, combined pairwise, then the lanes
+      float d0 = __fmul_rn(s[g][0], kk[0]), d1 = __fmul_rn(s[g][4], kk[4]);
+      float d2 = __fmul_rn(s[g][8], kk[8]), d3 = __fmul_rn(s[g][12], kk[12]);
+#pragma unroll
+      for (int e = 1; e < 4; ++e) {
+        d0 = __fmaf_rn(s[g][e], kk[e], d0);
+        d1 = __fmaf_rn(s[g][4 + e], kk[4 + e], d1);
+        d2 = __fmaf_rn(s[g][8 + e], kk[8 + e], d2);
+        d3 = __fmaf_rn(s[g][12 + e], kk[12 + e], d3);
+      }
+      float d = __fadd_rn(__fadd_rn(d0, d1), __fadd_rn(d2, d3));
+#pragma unroll
+      for (int off = LPR / 2; off >= 1; off >>= 1)
+        d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, off));
+      const int row_local = rows[g] - tile * VT;
+      const float vi = rows[g] < p.V ? v_s[t * VT + row_local] : 0.f;
+      const float u = __fmul_rn(be, __fsub_rn(vi, d));
+      // S = H + u khat^T
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s[g][e] = __fmaf_rn(u, kk[e], s[g][e]);
+      // o = S qhat
+      float o0 = __fmul_rn(s[g][0], qq[0]), o1 = __fmul_rn(s[g][4], qq[4]);
+      float o2 = __fmul_rn(s[g][8], qq[8]), o3 = __fmul_rn(s[g][12], qq[12]);
+#pragma unroll
+      for (int e = 1; e < 4; ++e) {
+        o0 = __fmaf_rn(s[g][e], qq[e], o0);
+        o1 = __fmaf_rn(s[g][4 + e], qq[4 + e], o1);
+        o2 = __fmaf_rn(s[g][8 + e], qq[8 + e], o2);
+        o3 = __fmaf_rn(s[g][12 + e], qq[12 + e], o3);
+      }
+      float o = __fadd_rn(__fadd_rn(o0, o1), __fadd_rn(o2, o3));
+#pragma unroll
+      for (int off = LPR / 2; off >= 1; off >>= 1)
+        o = __fadd_rn(o, __shfl_xor_sync(0xffffffffu, o, off));
+
+      if (rows[g] < p.V) {
+        if (l == 0) {
+          p.out[orow * p.out_stride + (size_t)h * p.V + rows[g]] = o;
+          if (!NATIVE) p.rec_u[(rec_base + t) * p.V + rows[g]] = u;
+        }
+        if (NATIVE) {
+          ST* snap = static_cast<ST*>(p.snaps) +
+                     (((size_t)r * p.W + t) * p.HV + h) * (size_t)p.V * K +
+                     (size_t)rows[g] * K;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            float x[4] = {s[g][4 * m], s[g][4 * m + 1], s[g][4 * m + 2], s[g][4 * m + 3]};
+            store_state4(snap + 4 * (l + LPR * m), x);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int K, typename QKV, typename ST, bool NATIVE>
+static int launch_one(const VerifyParams& p, cudaStream_t stream) {
+  using Tile = VerifyTile<K>;
+  const int ntiles = (p.V + Tile::VT - 1) / Tile::VT;
+  dim3 grid(ntiles * p.HV, p.batch);
+  const size_t smem = sizeof(float) * verify_smem_floats<K>(p.W);
+  gdn_verify_kernel<K, QKV, ST, NATIVE><<<grid, Tile::THREADS, smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <int K, bool NATIVE>
+static int dispatch_dtypes(const VerifyParams& p, int qkv_dtype, int state_dtype,
+                           cudaStream_t stream) {
+  if (qkv_dtype == GDN_DTYPE_F32 && state_dtype == GDN_DTYPE_F32)
+    return launch_one<K, float, float, NATIVE>(p, stream);
+  if (qkv_dtype == GDN_DTYPE_F32 && state_dtype == GDN_DTYPE_BF16)
+    return launch_one<K, float, __nv_bfloat16, NATIVE>(p, stream);
+  if (qkv_dtype == GDN_DTYPE_BF16 && state_dtype == GDN_DTYPE_F32)
+    return launch_one<K, __nv_bfloat16, float, NATIVE>(p, stream);
+  return launch_one<K, __nv_bfloat16, __nv_bfloat16, NATIVE>(p, stream);
+}
+
+int launch_verify(const VerifyParams& p, int head_k, int qkv_dtype, int state_dtype,
+                  bool native, cudaStream_t stream) {
+  switch (head_k) {
+#define GDN_CASE(KK)                                                              \
+  case KK:                                                                        \
+    return native ? dispatch_dtypes<KK, true>(p, qkv_dtype, state_dtype, stream)  \
+                  : dispatch_dtypes<KK, false>(p, qkv_dtype, state_dtype, stream);
+    GDN_CASE(16)
+    GDN_CASE(32)
+    GDN_CASE(64)
+    GDN_CASE(128)
+#undef GDN_CASE
+    default:
+      return GDN_ERR_UNSUPPORTED;
+  }
+}
+
+size_t verify_smem_bytes(int head_k, int W) {
+  switch (head_k) {
+    case 16: return sizeof(float) * verify_smem_floats<16>(W);
+    case 32: return sizeof(float) * verify_smem_floats<32>(W);
+    case 64: return sizeof(float) * verify_smem_floats<64>(W);
+    case 128: return sizeof(float) * verify_smem_floats<128>(W);
+    default: return 0;
+  }
+}
+
+int verify_rows_per_cta(int head_k) {
+  switch (head_k) {
+    case 16: return VerifyTile<16>::VT;
+    case 32: return VerifyTile<32>::VT;
+    case 64: return VerifyTile<64>::VT;
+    case 128: return VerifyTile<128>::VT;
+    default: return 0;
+  }
+}
+
+}  // namespace gdn

@@ -1,0 +1,71 @@
+"""One speculative step of an L-layer GDN stack through the C ABI.
+
+``StepBuffers`` owns the per-layer outputs and replay records of a
+``workloads.SpecBatch``; ``verify_all`` runs the verify of every layer
+(one launch per layer, as a model forward would), ``commit`` runs the
+single all-layer commit launch, and ``native_layer`` runs the native
+per-draft-snapshot baseline of one layer.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import api
+from .workloads import SpecBatch
+
+
+class StepBuffers:
+    def __init__(self, sb: SpecBatch, fill: Optional[float] = None):
+        dev = sb.device
+        make = (lambda shape: torch.full(shape, fill, dtype=torch.float32, device=dev)) \
+            if fill is not None else (lambda shape: torch.empty(shape, dtype=torch.float32, device=dev))
+        self.out = [make((sb.T, sb.HV, sb.V)) for _ in range(sb.L)]
+        self.rec_u = [make((sb.B, sb.HV, sb.W, sb.V)) for _ in range(sb.L)]
+        self.rec_k = [make((sb.B, sb.HV, sb.W, sb.K)) for _ in range(sb.L)]
+        self.rec_g = [make((sb.B, sb.HV, sb.W)) for _ in range(sb.L)]
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.table = api.LayerTable(sb.pools, self.rec_u, self.rec_k, self.rec_g)
+
+
+def verify_layer(sb: SpecBatch, bufs: StepBuffers, layer: int, stream=None) -> None:
+    api.gdn_spec_verify(
+        q=sb.q[layer], k=sb.k[layer], v=sb.v[layer], a=sb.a[layer], b=sb.b[layer],
+        A_log=sb.A_log[layer], dt_bias=sb.dt_bias[layer], token_start=sb.token_start,
+        window_len=sb.window_len, state_pool=sb.pools[layer], slot_table=sb.slot_table,
+        seq_pos=sb.seq_pos, block_size=sb.block_size, out=bufs.out[layer],
+        rec_u=bufs.rec_u[layer], rec_k=bufs.rec_k[layer], rec_g=bufs.rec_g[layer],
+        max_window=sb.W, err=bufs.err, stream=stream)
+
+
+def verify_all(sb: SpecBatch, bufs: StepBuffers, stream=None) -> None:
+    for layer in range(sb.L):
+        verify_layer(sb, bufs, layer, stream)
+
+
+def commit(sb: SpecBatch, bufs: StepBuffers, stream=None) -> None:
+    api.gdn_replay_commit(table=bufs.table, num_k_heads=sb.HK, window_len=sb.window_len,
+                          accepted_len=sb.accepted_len, slot_table=sb.slot_table,
+                          seq_pos=sb.seq_pos, block_size=sb.block_size, err=bufs.err,
+                          stream=stream)
+
+
+def native_layer(sb: SpecBatch, layer: int, out: torch.Tensor, snapshots: torch.Tensor,
+                 err: Optional[torch.Tensor] = None, stream=None) -> None:
+    api.gdn_native_spec_snapshot(
+        q=sb.q[layer], k=sb.k[layer], v=sb.v[layer], a=sb.a[layer], b=sb.b[layer],
+        A_log=sb.A_log[layer], dt_bias=sb.dt_bias[layer], token_start=sb.token_start,
+        window_len=sb.window_len, state_pool=sb.pools[layer], slot_table=sb.slot_table,
+        seq_pos=sb.seq_pos, block_size=sb.block_size, out=out, snapshots=snapshots,
+        max_window=sb.W, err=err, stream=stream)
+
+
+def native_buffers(sb: SpecBatch, fill: Optional[float] = None):
+    dev = sb.device
+    out = torch.empty((sb.T, sb.HV, sb.V), dtype=torch.float32, device=dev)
+    snaps = torch.empty((sb.B, sb.W, sb.HV, sb.V, sb.K), dtype=sb.state_dtype, device=dev)
+    if fill is not None:
+        out.fill_(fill)
+        snaps.fill_(fill)
+    return out, snaps

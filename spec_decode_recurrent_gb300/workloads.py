@@ -282,3 +282,41 @@ WORKLOADS = {
     "long_ragged": long_ragged,
     "align": align,
 }
+
+
+def custom(device="cpu", sentinel=True, seed=100, *, HK, HV, K, V, W, L, windows, accepted,
+           null_rows=(), num_slots=None, block_size=0, seq_pos=None, qkv_dtype=F32,
+           state_dtype=F32, gate_range=None, gaps=None, shuffle_rows=False, fused=False):
+    """A small step with explicit per-row windows / accepted lengths, for
+    parity cases the oracle runs in full.  Rows listed in null_rows get the
+    null slot.  In align mode (block_size > 0) seq_pos must be given and each
+    row gets distinct slots for every column its window can touch."""
+    cpu = _gen(seed, "cpu")
+    B = len(windows)
+    if block_size == 0:
+        need = B
+    else:
+        need = sum((p + W - 1) // block_size - (p - 1) // block_size + 1 for p in seq_pos)
+    num_slots = num_slots or need + 3
+    perm = torch.randperm(num_slots, generator=cpu).tolist()
+    tables, nxt = [], 0
+    for r in range(B):
+        if block_size == 0:
+            tables.append([perm[nxt]]); nxt += 1
+        else:
+            p0 = seq_pos[r]
+            row = [-1] * ((p0 + W - 1) // block_size + 1)
+            for col in range((p0 - 1) // block_size, (p0 + W - 1) // block_size + 1):
+                row[col] = perm[nxt]; nxt += 1
+            tables.append(row)
+        if r in null_rows:
+            tables[-1] = [-1] * len(tables[-1])
+    stride = max(len(t) for t in tables)
+    tables = [t + [-1] * (stride - len(t)) for t in tables]
+    order = torch.randperm(B, generator=cpu).tolist() if shuffle_rows else None
+    gen = _gen(seed, device)
+    return _make(f"custom{seed}", HK=HK, HV=HV, K=K, V=V, W=W, L=L, windows=list(windows),
+                 accepted=list(accepted), num_slots=num_slots, slots_for_row=tables,
+                 seq_pos=seq_pos, block_size=block_size, qkv_dtype=qkv_dtype,
+                 state_dtype=state_dtype, gen=gen, device=device, sentinel=sentinel,
+                 gate_range=gate_range, gaps=gaps, row_order=order, fused=fused)

@@ -1,0 +1,231 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle and
+against the GPU native per-draft-snapshot kernel.
+
+* small steps (oracle runs everything): every output element, record entry
+  and committed state within tolerance, and untouched entries untouched;
+* full-size workloads in the launch configuration the benchmark times:
+  verify == native and commit == native snapshot n bit for bit over every
+  layer, row and head (plus no stray pool writes), and sampled (layer, row,
+  head) units recomputed by the oracle.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from spec_decode_recurrent_gb300 import api, build, step, workloads as wl
+from tests._parity import GpuStep, compare_full, oracle_full
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    api.load()
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ small steps
+def test_tiny_config_full_oracle():
+    sb = wl.tiny(device="cuda")
+    gs = GpuStep(sb)
+    assert gs.err == 0 and gs.verify_err == 0
+    gs.check_bitwise()
+    layers, pools, err = oracle_full(sb)
+    assert np.all(err == 0)
+    compare_full(gs, layers, pools)
+
+
+SMALL = {
+    # several 32-row tiles, ragged windows incl. decode-only (1) and padding (0),
+    # a null-slot row, strided fused q/k/v, permuted rows with gaps
+    "ragged_fp32": dict(HK=2, HV=4, K=128, V=128, W=6, L=2, windows=[6, 4, 1, 3, 0, 6, 2],
+                        accepted=[3, 4, 1, 2, 0, 6, 1], null_rows=(5,), gaps=[1, 0, 2, 3, 0, 1, 0],
+                        shuffle_rows=True, fused=True),
+    "ragged_bf16_qkv": dict(HK=2, HV=4, K=128, V=128, W=6, L=2, windows=[6, 4, 1, 3, 0, 6, 2],
+                            accepted=[6, 1, 1, 3, 0, 2, 5], gaps=[0, 2, 1, 0, 3, 1, 2],
+                            shuffle_rows=True, fused=True, qkv_dtype=wl.BF16),
+    "extreme_gates": dict(HK=1, HV=2, K=128, V=128, W=6, L=1, windows=[6, 6, 5, 1],
+                          accepted=[6, 3, 5, 1], gate_range=20.0, qkv_dtype=wl.BF16),
+    "bf16_state": dict(HK=2, HV=4, K=128, V=128, W=4, L=2, windows=[4, 4, 2, 0],
+                       accepted=[4, 1, 2, 0], qkv_dtype=wl.BF16, state_dtype=wl.BF16),
+    "gqa4_k64_v32": dict(HK=1, HV=4, K=64, V=32, W=5, L=2, windows=[5, 3, 5], accepted=[2, 3, 5]),
+    "k32_v64": dict(HK=3, HV=6, K=32, V=64, W=4, L=1, windows=[4, 2], accepted=[1, 2]),
+    "k16_v128": dict(HK=1, HV=1, K=16, V=128, W=3, L=1, windows=[3, 3], accepted=[3, 2]),
+    "k128_v16": dict(HK=1, HV=2, K=128, V=16, W=3, L=1, windows=[3, 1], accepted=[2, 1]),
+    "max_window16": dict(HK=1, HV=2, K=128, V=128, W=16, L=1, windows=[16, 9, 16],
+                         accepted=[16, 9, 7]),
+    "align_fp32": dict(HK=2, HV=4, K=128, V=128, W=4, L=2, windows=[4] * 8,
+                       accepted=[1, 2, 3, 4, 4, 4, 2, 3], block_size=4,
+                       seq_pos=[4, 5, 6, 7, 8, 9, 10, 11]),
+    "align_bf16_state": dict(HK=2, HV=4, K=128, V=128, W=4, L=2, windows=[4] * 8,
+                             accepted=[4, 3, 2, 1, 4, 4, 2, 3], block_size=4,
+                             seq_pos=[4, 5, 6, 7, 8, 9, 10, 11], qkv_dtype=wl.BF16,
+                             state_dtype=wl.BF16),
+    "align_multi_boundary": dict(HK=1, HV=2, K=128, V=128, W=16, L=1, windows=[16, 16, 9, 12],
+                                 accepted=[16, 13, 9, 12], block_size=4, seq_pos=[5, 8, 3, 1]),
+    "align_block3_w6": dict(HK=1, HV=2, K=64, V=64, W=6, L=2, windows=[6, 6, 6, 3],
+                            accepted=[6, 5, 3, 3], block_size=3, seq_pos=[1, 2, 3, 7]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_step_full_oracle(name):
+    sb = wl.custom(device="cuda", **SMALL[name])
+    gs = GpuStep(sb)
+    assert gs.err == 0 and gs.verify_err == 0
+    gs.check_bitwise()
+    layers, pools, err = oracle_full(sb)
+    assert np.all(err == 0)
+    compare_full(gs, layers, pools)
+
+
+# ------------------------------------------------------- full-size workloads
+FULL = {
+    "layer": lambda: wl.layer(device="cuda"),
+    "all_layer": lambda: wl.all_layer(device="cuda"),
+    "long_ragged_seed30": lambda: wl.long_ragged(device="cuda", seed=30),
+    "long_ragged_seed31": lambda: wl.long_ragged(device="cuda", seed=31),
+    "long_ragged_seed32": lambda: wl.long_ragged(device="cuda", seed=32),
+    "align_fp32": lambda: wl.align(device="cuda"),
+    "align_bf16": lambda: wl.align(device="cuda", state_dtype=wl.BF16),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_workload(name):
+    sb = FULL[name]()
+    try:
+        gs = GpuStep(sb)
+        assert gs.err == 0 and gs.verify_err == 0
+        gs.check_bitwise()
+        for l, r, h in gs.units(12, seed=len(name)):
+            gs.check_unit_against_oracle(l, r, h)
+    finally:
+        del sb
+        _free()
+
+
+# ------------------------------------------------------------- edge cases
+def test_identity_gates_commit_leaves_state_bitwise():
+    sb = wl.custom(device="cuda", HK=1, HV=2, K=128, V=128, W=4, L=2, windows=[4, 3],
+                   accepted=[4, 2])
+    for l in range(sb.L):
+        sb.a[l].fill_(-1e4)     # softplus -> 0: decay 1
+        sb.b[l].fill_(-1e4)     # sigmoid -> 0: no write
+    gs = GpuStep(sb)
+    for l in range(sb.L):
+        assert torch.equal(sb.pools[l].view(torch.int32), gs.before[l].view(torch.int32))
+        assert torch.count_nonzero(gs.bufs.rec_u[l][:, :, :3]) == 0
+
+
+def test_accepted_zero_and_padding_rows_write_nothing():
+    sb = wl.custom(device="cuda", HK=1, HV=2, K=64, V=64, W=4, L=2, windows=[4, 0, 4, 4],
+                   accepted=[0, 0, 0, 2], null_rows=(2,))
+    gs = GpuStep(sb)
+    assert gs.err == 0
+    gs.check_bitwise()
+    for l in range(sb.L):
+        # only row 3's slot may change
+        changed = (sb.pools[l].view(torch.int32) != gs.before[l].view(torch.int32))
+        slots = changed.flatten(1).any(1).nonzero().flatten().tolist()
+        assert slots == [int(sb.slot_table[3, 0])]
+        # the null row and the empty row wrote no outputs or records
+        t0 = int(sb.token_start[2])
+        assert torch.isnan(gs.bufs.out[l][t0:t0 + 4]).all()
+        assert torch.isnan(gs.bufs.rec_u[l][1:3]).all()
+
+
+def test_empty_batch_is_a_no_op():
+    sb = wl.custom(device="cuda", HK=1, HV=2, K=64, V=64, W=4, L=1, windows=[4], accepted=[2])
+    e = torch.empty(0, dtype=torch.int32, device="cuda")
+    bufs = step.StepBuffers(sb, fill=float("nan"))
+    api.gdn_spec_verify(q=sb.q[0], k=sb.k[0], v=sb.v[0], a=sb.a[0], b=sb.b[0], A_log=sb.A_log[0],
+                        dt_bias=sb.dt_bias[0], token_start=e, window_len=e,
+                        state_pool=sb.pools[0], slot_table=e.view(0, 1), out=bufs.out[0],
+                        rec_u=bufs.rec_u[0][:0], rec_k=bufs.rec_k[0][:0], rec_g=bufs.rec_g[0][:0],
+                        max_window=sb.W)
+    torch.cuda.synchronize()
+    assert torch.isnan(bufs.out[0]).all()
+
+
+def test_malformed_rows_are_flagged_and_skipped():
+    # rows: fine | accepted > window | slot out of range | window > W | token rows past T
+    sb = wl.custom(device="cuda", HK=1, HV=2, K=64, V=64, W=4, L=1, windows=[4, 2, 3, 4, 2],
+                   accepted=[2, 1, 1, 1, 1])
+    sb.accepted_len[1] = 3
+    sb.slot_table[2, 0] = sb.num_slots + 5
+    sb.window_len[3] = 5
+    sb.token_start[4] = sb.T - 1
+    sb.accepted_len[4] = 0        # a caller commits nothing for a row its verify rejected
+    gs = GpuStep(sb, native=False)
+    assert gs.verify_err == api.ROW_ERR_SLOT | api.ROW_ERR_WINDOW | api.ROW_ERR_TOKENS
+    assert gs.err == (api.ROW_ERR_SLOT | api.ROW_ERR_WINDOW | api.ROW_ERR_TOKENS
+                      | api.ROW_ERR_ACCEPTED)
+    changed = (sb.pools[0].view(torch.int32) != gs.before[0].view(torch.int32))
+    slots = changed.flatten(1).any(1).nonzero().flatten().tolist()
+    assert slots == [int(sb.slot_table[0, 0])]
+
+
+def test_align_missing_block_is_flagged():
+    sb = wl.custom(device="cuda", HK=1, HV=2, K=64, V=64, W=4, L=1, windows=[4, 4],
+                   accepted=[4, 4], block_size=4, seq_pos=[6, 4])
+    final_col = (6 + 4 - 1) // 4
+    sb.slot_table[0, final_col] = -1
+    gs = GpuStep(sb, native=False)
+    assert gs.verify_err == 0
+    assert gs.err == api.ROW_ERR_BLOCK
+
+
+def test_host_validation_rejects_bad_arguments():
+    sb = wl.custom(device="cuda", HK=1, HV=2, K=64, V=64, W=4, L=1, windows=[4], accepted=[2])
+    bufs = step.StepBuffers(sb)
+    kw = dict(q=sb.q[0], k=sb.k[0], v=sb.v[0], a=sb.a[0], b=sb.b[0], A_log=sb.A_log[0],
+              dt_bias=sb.dt_bias[0], token_start=sb.token_start, window_len=sb.window_len,
+              state_pool=sb.pools[0], slot_table=sb.slot_table, out=bufs.out[0],
+              rec_u=bufs.rec_u[0], rec_k=bufs.rec_k[0], rec_g=bufs.rec_g[0], max_window=sb.W)
+    with pytest.raises(api.GDNError) as e:
+        api.gdn_spec_verify(**dict(kw, max_window=17, rec_u=torch.zeros(1, 2, 17, 64, device="cuda"),
+                                   rec_k=torch.zeros(1, 2, 17, 64, device="cuda"),
+                                   rec_g=torch.zeros(1, 2, 17, device="cuda")))
+    assert e.value.code == -2
+    with pytest.raises(api.GDNError) as e:       # negative block size
+        api.gdn_spec_verify(**dict(kw, block_size=-1, seq_pos=sb.window_len))
+    assert e.value.code == -3
+    with pytest.raises(api.GDNError) as e:       # a row stride shorter than a row
+        api.gdn_spec_verify(**dict(kw, q=sb.q[0].as_strided(sb.q[0].shape, (32, 64, 1))))
+    assert e.value.code == -3
+
+
+def test_align_commit_repeatable_bitwise():
+    # A boundary slot can be the checkpoint slot; the commit must not read a
+    # tile another CTA already overwrote.  Run the same commit 20 times from
+    # the same checkpoint and require identical results.
+    sb = wl.align(device="cuda", L=4, batch=128)
+    bufs = step.StepBuffers(sb)
+    step.verify_all(sb, bufs)
+    before = [p.clone() for p in sb.pools]
+    results = None
+    for _ in range(20):
+        for p, b in zip(sb.pools, before):
+            p.copy_(b)
+        step.commit(sb, bufs)
+        torch.cuda.synchronize()
+        now = [p.view(torch.int32).clone() for p in sb.pools]
+        if results is None:
+            results = now
+        else:
+            for a, b in zip(results, now):
+                assert torch.equal(a, b)
+    assert int(bufs.err.item()) == 0
