@@ -35,6 +35,8 @@
  *   - Return value: GDN_OK, or a negative GDN_ERR_* for a problem the host
  *     can see (null pointer, unsupported shape, bad stride or alignment,
  *     failed launch).  Nothing is launched when the return is negative.
+ *     batch == 0 launches nothing and checks only the shape (the per-row
+ *     arrays of an empty batch may be NULL).
  *   - Row-level problems are found on the device: the row is skipped (it
  *     writes nothing) and its GDN_ROW_ERR_* bits are OR-ed into *err when
  *     err is not NULL.  The caller clears *err beforehand.

@@ -108,6 +108,7 @@ int gdn_spec_verify(const gdn_shape* shape, int32_t batch, int32_t num_tokens,
                     int32_t block_size, float* out, int64_t out_row_stride,
                     float* rec_u, float* rec_k, float* rec_g, int32_t* err,
                     void* stream) {
+  if (batch == 0) return check_shape(shape);  // nothing to do; row arrays may be empty
   gdn::VerifyParams p;
   int rc = prepare_verify(&p, shape, batch, num_tokens, num_slots, q, q_row_stride, k,
                           k_row_stride, v, v_row_stride, a, b, A_log, dt_bias, token_start,
@@ -133,6 +134,7 @@ int gdn_native_spec_snapshot(
     const void* state_pool, const int32_t* slot_table, int32_t slot_table_stride,
     const int32_t* seq_pos, int32_t block_size, float* out, int64_t out_row_stride,
     void* snapshots, int32_t* err, void* stream) {
+  if (batch == 0) return check_shape(shape);
   gdn::VerifyParams p;
   int rc = prepare_verify(&p, shape, batch, num_tokens, num_slots, q, q_row_stride, k,
                           k_row_stride, v, v_row_stride, a, b, A_log, dt_bias, token_start,
@@ -156,7 +158,7 @@ int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
                       const int32_t* seq_pos, int32_t block_size, int32_t* err,
                       void* stream) {
   int rc = check_shape(shape);
-  if (rc != GDN_OK) return rc;
+  if (rc != GDN_OK || batch == 0) return rc;
   if (!state_pools || !rec_u || !rec_k || !rec_g || !window_len || !accepted_len || !slot_table)
     return GDN_ERR_NULL;
   if (block_size < 0 || slot_table_stride < 1) return GDN_ERR_INVALID;

@@ -82,8 +82,7 @@ class SpecBatch:
 def sentinel_like(shape, dtype, device) -> torch.Tensor:
     if dtype == F32:
         return torch.full(shape, SENTINEL_F32_BITS, dtype=torch.int32, device=device).view(F32)
-    bits = SENTINEL_BF16_BITS - 0x10000  # as a signed int16
-    return torch.full(shape, bits, dtype=torch.int16, device=device).view(BF16)
+    return torch.full(shape, SENTINEL_BF16_BITS, dtype=torch.int16, device=device).view(BF16)
 
 
 def _uniform(shape, lo, hi, gen, device):

@@ -116,19 +116,20 @@ class GpuStep:
                 check_bf16(got, want, f"{tag}: bf16 state after {ntok} tokens")
 
 
-def oracle_full(sb):
-    """Run the oracle on the whole (small) step: verify with snapshots per
-    layer, then the all-layer commit from the oracle's own records."""
+def oracle_full(sb, pools_before):
+    """Run the oracle on the whole (small) step from the checkpoint pools as
+    they were before the GPU commit: verify with snapshots per layer, then
+    the all-layer commit from the oracle's own records."""
     sp = None if sb.seq_pos is None else sb.seq_pos.cpu()
     layers = []
     for l in range(sb.L):
         layers.append(oracle.spec_verify(
             q=sb.q[l].cpu(), k=sb.k[l].cpu(), v=sb.v[l].cpu(), a=sb.a[l].cpu(), b=sb.b[l].cpu(),
             A_log=sb.A_log[l].cpu(), dt_bias=sb.dt_bias[l].cpu(), token_start=sb.token_start.cpu(),
-            window_len=sb.window_len.cpu(), pool=sb.pools[l].cpu(), slot_table=sb.slot_table.cpu(),
+            window_len=sb.window_len.cpu(), pool=pools_before[l].cpu(), slot_table=sb.slot_table.cpu(),
             seq_pos=sp, block_size=sb.block_size, max_window=sb.W, snapshots=True))
     pools, err = oracle.replay_commit(
-        pools=np.stack([cpu64(p) for p in sb.pools]),
+        pools=np.stack([cpu64(p) for p in pools_before]),
         rec_u=np.stack([x["rec_u"] for x in layers]), rec_k=np.stack([x["rec_k"] for x in layers]),
         rec_g=np.stack([x["rec_g"] for x in layers]), window_len=sb.window_len.cpu(),
         accepted_len=sb.accepted_len.cpu(), slot_table=sb.slot_table.cpu(), seq_pos=sp,

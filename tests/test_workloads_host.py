@@ -1,0 +1,77 @@
+"""CPU checks of the seeded input generators and of the host side of the
+parity harness and the benchmark (no GPU): every workload the GPU tests and
+the benchmark use can be drawn, is well formed, and the oracle runs on it."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from spec_decode_recurrent_gb300 import roofline, workloads as wl
+from tests import test_gpu_parity as gp
+from tests._parity import oracle_full, row_plan
+
+
+def _check_layout(sb):
+    assert sb.token_start.shape == (sb.B,) and sb.window_len.shape == (sb.B,)
+    for r in range(sb.B):
+        w, t0 = int(sb.window_len[r]), int(sb.token_start[r])
+        assert 0 <= t0 and t0 + w <= sb.T
+        src, writes = row_plan(sb, r)
+        if w > 0 and src >= 0:
+            pool = sb.pools[0][src].float()
+            assert torch.isfinite(pool).all(), f"row {r} reads a sentinel slot"
+        for slot, ntok in writes:
+            assert 0 <= slot < sb.num_slots and 1 <= ntok <= int(sb.accepted_len[r])
+    # no two live rows share a written slot
+    seen = set()
+    for r in range(sb.B):
+        for slot, _ in row_plan(sb, r)[1]:
+            assert slot not in seen
+            seen.add(slot)
+
+
+@pytest.mark.parametrize("name", sorted(gp.SMALL))
+def test_small_cases_generate_and_run_on_the_oracle(name):
+    sb = wl.custom(device="cpu", **gp.SMALL[name])
+    _check_layout(sb)
+    layers, pools, err = oracle_full(sb, sb.pools)
+    assert np.all(err == 0)
+    assert all(np.isfinite(x["out"][~np.isnan(x["out"])]).all() for x in layers)
+
+
+def test_named_workloads_generate_small():
+    for sb in (wl.tiny(), wl.layer(batch=4, HK=2, HV=4, KV=16, num_slots=8),
+               wl.all_layer(L=2, batch=10, pad_rows=2, HK=2, HV=4, KV=16, num_slots=16),
+               wl.long_ragged(L=2, batch=12, HK=2, HV=4, KV=16, num_slots=24),
+               wl.align(L=2, batch=16, HK=2, HV=4, KV=16, num_slots=40),
+               wl.align(L=1, batch=16, HK=2, HV=4, KV=16, num_slots=40, state_dtype=wl.BF16)):
+        _check_layout(sb)
+        assert roofline.commit_bytes(sb) > 0 and roofline.verify_bytes_per_layer(sb) > 0
+
+
+def test_align_workload_covers_every_boundary_case():
+    sb = wl.align(L=1, batch=128, HK=1, HV=1, KV=16, num_slots=384)
+    pairs = {(int(p) % 4, int(n)) for p, n in zip(sb.seq_pos, sb.accepted_len)}
+    assert pairs == {(r, n) for r in range(4) for n in range(1, 5)}
+    same = 0
+    for r in range(sb.B):
+        src, writes = row_plan(sb, r)
+        same += any(s == src for s, _ in writes[1:])
+    assert same > 0          # some boundary writes land in the checkpoint slot
+
+
+def test_sentinels_are_nan_bit_patterns():
+    f = wl.sentinel_like((3,), wl.F32, "cpu")
+    b = wl.sentinel_like((3,), wl.BF16, "cpu")
+    assert torch.isnan(f).all() and torch.isnan(b.float()).all()
+    assert f.view(torch.int32)[0].item() == wl.SENTINEL_F32_BITS
+    assert b.view(torch.int16)[0].item() == wl.SENTINEL_BF16_BITS
+
+
+def test_bench_cpu_baseline_helpers_run_on_cpu():
+    import bench
+    sb = wl.all_layer(L=2, batch=6, pad_rows=1, HK=2, HV=4, KV=16, num_slots=12, sentinel=False)
+    d = bench._compact_layer(sb, 0, list(range(sb.B)))
+    bench._oracle_unit_of_work(oracle, d, sb)
+    res = bench.cpu_baseline(sb, 0.01)
+    assert res["value"] > 0 and res["cores"] >= 1
