@@ -137,6 +137,38 @@ __device__ __forceinline__ void store_state4(__nv_bfloat16* p, const float (&x)[
   __stcs(reinterpret_cast<uint2*>(p), t);
 }
 
+// ------------------------------------------------ packed fp32 pairs (sm_100+)
+// Two floats in one 64-bit register, operated on by the packed fp32
+// instructions (mul.rn.f32x2 / fma.rn.f32x2 / add.rn.f32x2).  Each lane is
+// rounded exactly as the scalar __fmul_rn / __fmaf_rn / __fadd_rn would
+// round it, so packing changes the instruction count, never a result.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(f32x2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// The commit's fold on a pair: fma(u, khat, S * alpha) per lane.
+__device__ __forceinline__ f32x2 fold2(f32x2 s, f32x2 alpha, f32x2 u, f32x2 kh) {
+  return fma2(u, kh, mul2(s, alpha));
+}
+
 // --------------------------------------------------------- the recurrence
 // One element's decay-then-write, the commit's fold and the verify's state
 // update: S = fma(u, khat, S * alpha).

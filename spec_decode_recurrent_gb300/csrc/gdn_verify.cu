@@ -1,11 +1,12 @@
 // gdn_verify.cu -- speculative verify and native per-draft snapshot kernels.
 //
-// One CTA of 4 warps owns a tile of VT state rows of one (request row,
-// value head) and runs the whole draft window over it with the tile held in
-// registers (tokenspeed PR "feat: add Qwen3.5 GDN ReplaySSM", Summary and
-// Implementation: a cooperative 4-warp CTA per 128x128 state head; here the
-// head is additionally split into V tiles so that small batches still fill
-// 152 SMs).  Rows of S are independent given (khat, qhat, alpha, beta, v_i),
+// One CTA of 8 warps owns a tile of VT state rows (64 for K = 128) of one
+// (request row, value head) and runs the whole draft window over it with
+// the tile held in registers (tokenspeed PR "feat: add Qwen3.5 GDN
+// ReplaySSM", Summary and Implementation: a cooperative multi-warp CTA per
+// 128x128 state head; here a head is split into V tiles so that small
+// batches still fill 152 SMs, and a tile is wide enough that the per-token
+// staging -- key/query norms, gates -- is shared by many rows).  Rows of S are independent given (khat, qhat, alpha, beta, v_i),
 // so tiles never communicate; the only reductions are over K, inside a
 // group of K/16 lanes, by warp shuffles.
 //
@@ -30,7 +31,7 @@ struct VerifyTile {
   static constexpr int LPR = K / 16;          // lanes per state row
   static constexpr int RPW = 32 / LPR;        // rows per warp per row group
   static constexpr int RPT = (K == 128) ? 2 : 1;  // row groups per thread
-  static constexpr int WARPS = 4;
+  static constexpr int WARPS = 8;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int VT = WARPS * RPW * RPT;    // state rows per CTA
   static constexpr int CPL = 16;              // columns per lane
@@ -80,7 +81,9 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
   // ---- the token inputs are staged
   const ST* S0 = static_cast<const ST*>(p.pool) +
                  ((size_t)src.slot * p.HV + h) * (size_t)p.V * K;
-  float s[RPT][16];
+  // tile row group g holds columns 4*(l + LPR*m) + {0..3}, m = 0..3, as
+  // eight packed pairs: s[g][2m] = columns +0,+1 and s[g][2m+1] = +2,+3
+  f32x2 s[RPT][8];
   int rows[RPT];
 #pragma unroll
   for (int g = 0; g < RPT; ++g) {
@@ -90,12 +93,12 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
       for (int m = 0; m < 4; ++m) {
         float x[4];
         load_state4(S0 + (size_t)rows[g] * K + 4 * (l + LPR * m), x);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[g][4 * m + e] = x[e];
+        s[g][2 * m] = pack2(x[0], x[1]);
+        s[g][2 * m + 1] = pack2(x[2], x[3]);
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) s[g][e] = 0.0f;
+      for (int j = 0; j < 8; ++j) s[g][j] = 0ull;
     }
   }
 
@@ -126,14 +129,16 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
       ks = __fadd_rn(ks, __shfl_xor_sync(0xffffffffu, ks, off));
       qs = __fadd_rn(qs, __shfl_xor_sync(0xffffffffu, qs, off));
     }
-    const float kn = __fsqrt_rn(__fadd_rn(ks, kL2NormEps));
-    const float qn = __fsqrt_rn(__fadd_rn(qs, kL2NormEps));
+    // x / sqrt(|x|^2 + eps) as x * rsqrt(|x|^2 + eps), rsqrt correctly rounded
+    const float kr = __frsqrt_rn(__fadd_rn(ks, kL2NormEps));
+    const float qr = __frsqrt_rn(__fadd_rn(qs, kL2NormEps));
     if (lane < K / 4) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kh_s[t * K + 4 * lane + e] = __fdiv_rn(kx[e], kn);
-        qh_s[t * K + 4 * lane + e] = __fdiv_rn(qx[e], qn);
-      }
+      *reinterpret_cast<float4*>(kh_s + t * K + 4 * lane) =
+          make_float4(__fmul_rn(kx[0], kr), __fmul_rn(kx[1], kr), __fmul_rn(kx[2], kr),
+                      __fmul_rn(kx[3], kr));
+      *reinterpret_cast<float4*>(qh_s + t * K + 4 * lane) =
+          make_float4(__fmul_rn(qx[0], qr), __fmul_rn(qx[1], qr), __fmul_rn(qx[2], qr),
+                      __fmul_rn(qx[3], qr));
     }
     for (int i = lane; i < VT; i += 32) {
       const int row = tile * VT + i;
@@ -156,32 +161,32 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
 
   // ---- the draft window, token by token, state in registers
   for (int t = 0; t < w; ++t) {
-    const float al = al_s[t], be = be_s[t];
-    float kk[16], qq[16];
+    const float be = be_s[t];
+    const f32x2 al2 = pack2(al_s[t], al_s[t]);
+    f32x2 kk[8], qq[8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const float4 k4 = *reinterpret_cast<const float4*>(kh_s + t * K + 4 * (l + LPR * m));
-      const float4 q4 = *reinterpret_cast<const float4*>(qh_s + t * K + 4 * (l + LPR * m));
-      kk[4 * m + 0] = k4.x; kk[4 * m + 1] = k4.y; kk[4 * m + 2] = k4.z; kk[4 * m + 3] = k4.w;
-      qq[4 * m + 0] = q4.x; qq[4 * m + 1] = q4.y; qq[4 * m + 2] = q4.z; qq[4 * m + 3] = q4.w;
+      const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kh_s + t * K + 4 * (l + LPR * m));
+      const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(qh_s + t * K + 4 * (l + LPR * m));
+      kk[2 * m] = k4.x; kk[2 * m + 1] = k4.y;
+      qq[2 * m] = q4.x; qq[2 * m + 1] = q4.y;
     }
     const long long orow = t0 + t;
 #pragma unroll
     for (int g = 0; g < RPT; ++g) {
       // H = alpha * S
 #pragma unroll
-      for (int e = 0; e < 16; ++e) s[g][e] = __fmul_rn(s[g][e], al);
-      // d = H khat: four chunk partials, combined pairwise, then the lanes
-      float d0 = __fmul_rn(s[g][0], kk[0]), d1 = __fmul_rn(s[g][4], kk[4]);
-      float d2 = __fmul_rn(s[g][8], kk[8]), d3 = __fmul_rn(s[g][12], kk[12]);
+      for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], al2);
+      // d = H khat: two pair accumulators (pairs 0-3, 4-7), their four
+      // lanes summed in a fixed order, then the LPR lanes of the row
+      f32x2 da = mul2(s[g][0], kk[0]), db = mul2(s[g][4], kk[4]);
 #pragma unroll
-      for (int e = 1; e < 4; ++e) {
-        d0 = __fmaf_rn(s[g][e], kk[e], d0);
-        d1 = __fmaf_rn(s[g][4 + e], kk[4 + e], d1);
-        d2 = __fmaf_rn(s[g][8 + e], kk[8 + e], d2);
-        d3 = __fmaf_rn(s[g][12 + e], kk[12 + e], d3);
+      for (int j = 1; j < 4; ++j) {
+        da = fma2(s[g][j], kk[j], da);
+        db = fma2(s[g][4 + j], kk[4 + j], db);
       }
-      float d = __fadd_rn(__fadd_rn(d0, d1), __fadd_rn(d2, d3));
+      const float2 fa = unpack2(da), fb = unpack2(db);
+      float d = __fadd_rn(__fadd_rn(fa.x, fa.y), __fadd_rn(fb.x, fb.y));
 #pragma unroll
       for (int off = LPR / 2; off >= 1; off >>= 1)
         d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, off));
@@ -189,19 +194,18 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
       const float vi = rows[g] < p.V ? v_s[t * VT + row_local] : 0.f;
       const float u = __fmul_rn(be, __fsub_rn(vi, d));
       // S = H + u khat^T
+      const f32x2 u2 = pack2(u, u);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) s[g][e] = __fmaf_rn(u, kk[e], s[g][e]);
+      for (int j = 0; j < 8; ++j) s[g][j] = fma2(u2, kk[j], s[g][j]);
       // o = S qhat
-      float o0 = __fmul_rn(s[g][0], qq[0]), o1 = __fmul_rn(s[g][4], qq[4]);
-      float o2 = __fmul_rn(s[g][8], qq[8]), o3 = __fmul_rn(s[g][12], qq[12]);
+      f32x2 oa = mul2(s[g][0], qq[0]), ob = mul2(s[g][4], qq[4]);
 #pragma unroll
-      for (int e = 1; e < 4; ++e) {
-        o0 = __fmaf_rn(s[g][e], qq[e], o0);
-        o1 = __fmaf_rn(s[g][4 + e], qq[4 + e], o1);
-        o2 = __fmaf_rn(s[g][8 + e], qq[8 + e], o2);
-        o3 = __fmaf_rn(s[g][12 + e], qq[12 + e], o3);
+      for (int j = 1; j < 4; ++j) {
+        oa = fma2(s[g][j], qq[j], oa);
+        ob = fma2(s[g][4 + j], qq[4 + j], ob);
       }
-      float o = __fadd_rn(__fadd_rn(o0, o1), __fadd_rn(o2, o3));
+      const float2 ga = unpack2(oa), gb = unpack2(ob);
+      float o = __fadd_rn(__fadd_rn(ga.x, ga.y), __fadd_rn(gb.x, gb.y));
 #pragma unroll
       for (int off = LPR / 2; off >= 1; off >>= 1)
         o = __fadd_rn(o, __shfl_xor_sync(0xffffffffu, o, off));
@@ -217,7 +221,8 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
                      (size_t)rows[g] * K;
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
-            float x[4] = {s[g][4 * m], s[g][4 * m + 1], s[g][4 * m + 2], s[g][4 * m + 3]};
+            const float2 a = unpack2(s[g][2 * m]), b = unpack2(s[g][2 * m + 1]);
+            const float x[4] = {a.x, a.y, b.x, b.y};
             store_state4(snap + 4 * (l + LPR * m), x);
           }
         }
