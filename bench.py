@@ -181,6 +181,7 @@ def run_gpu(args, rank, local_rank, world_size):
     api.load()
     sd = torch.bfloat16 if args.state_dtype == "bf16" else torch.float32
     sb = make_workload(args.workload, dev, rank, sd, args.layers)
+    arena = step.pack_inputs(sb)   # one contiguous buffer of the step's inputs
     bufs = step.StepBuffers(sb)
     stream = torch.cuda.current_stream()
 
@@ -252,7 +253,7 @@ def run_gpu(args, rank, local_rank, world_size):
     nbytes = roofline.native_bytes_per_layer(sb)
     del out_n, snaps
 
-    e2e = None if args.no_e2e else run_e2e(args, sb, bufs, graph, stream)
+    e2e = None if args.no_e2e else run_e2e(args, sb, bufs, graph, stream, arena)
 
     result = {
         "metric": METRIC, "value": round(ms_per_step * 1e3, 3), "unit": UNIT,
@@ -300,31 +301,23 @@ def run_gpu(args, rank, local_rank, world_size):
     return result
 
 
-def run_e2e(args, sb, bufs, graph, stream):
+def run_e2e(args, sb, bufs, graph, stream, arena):
     """The same step through the public API with host buffers: every step
-    copies its inputs from pinned host memory, runs, and reads back the
-    outputs of every layer and the error word."""
-    ins = []
-    for l in range(sb.L):
-        srcs = sb.fused_qkv[l:l + 1] if sb.fused_qkv else [sb.q[l], sb.k[l], sb.v[l]]
-        for t in srcs + [sb.a[l], sb.b[l]]:
-            ins.append(t)
-    ins += [sb.token_start, sb.window_len, sb.accepted_len, sb.slot_table]
-    if sb.seq_pos is not None:
-        ins.append(sb.seq_pos)
-    host_in = [t.cpu().pin_memory() for t in ins]
-    outs = bufs.out + [bufs.err]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    bi = sum(t.numel() * t.element_size() for t in host_in)
-    bo = sum(t.numel() * t.element_size() for t in host_out)
+    copies all of its inputs (q/k/v, gates, row metadata of every layer)
+    from pinned host memory in one copy, runs, and reads back every layer's
+    output and the error word."""
+    host_in = arena.cpu().pin_memory()
+    host_out = torch.empty(bufs.out_all.shape, dtype=torch.float32, pin_memory=True)
+    host_err = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    bi = host_in.numel()
+    bo = host_out.numel() * 4 + 4
 
     def one():
-        for d, h in zip(ins, host_in):
-            d.copy_(h, non_blocking=True)
+        arena.copy_(host_in, non_blocking=True)
         graph.replay()
         step.commit(sb, bufs)
-        for h, d in zip(host_out, outs):
-            h.copy_(d, non_blocking=True)
+        host_out.copy_(bufs.out_all, non_blocking=True)
+        host_err.copy_(bufs.err, non_blocking=True)
 
     for _ in range(3):
         one()
@@ -340,8 +333,8 @@ def run_e2e(args, sb, bufs, graph, stream):
     ms = dist.max_over_ranks(a.elapsed_time(b), torch.cuda.current_device()) / E
     return {"value": round(ms * 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "steps": E,
-            "path": "pinned host -> device copies, verify graph + commit call, device -> host "
-                    "copies of every layer's output and the error word"}
+            "path": "one pinned host -> device copy of every input of the step, verify graph + "
+                    "commit call, one device -> host copy of every layer's output, error word"}
 
 
 # ---------------------------------------------------- CPU oracle timing

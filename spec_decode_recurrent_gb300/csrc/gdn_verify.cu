@@ -140,15 +140,17 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
           make_float4(__fmul_rn(qx[0], qr), __fmul_rn(qx[1], qr), __fmul_rn(qx[2], qr),
                       __fmul_rn(qx[3], qr));
     }
-    for (int i = lane; i < VT; i += 32) {
-      const int row = tile * VT + i;
-      v_s[t * VT + i] = row < p.V ? load1(vb + row_t * p.v_stride + (size_t)h * p.V + row) : 0.f;
-    }
-    if (lane == 0) {
-      const size_t gi = (size_t)row_t * p.HV + h;
-      al_s[t] = gate_decay(p.a[gi], p.A_log[h], p.dt_bias[h]);
-      be_s[t] = gate_beta(p.b[gi]);
-    }
+  }
+  // gates of the whole window: one lane per token in the last warp
+  if (warp == Tile::WARPS - 1 && lane < w) {
+    const size_t gi = (size_t)(t0 + lane) * p.HV + h;
+    al_s[lane] = gate_decay(p.a[gi], p.A_log[h], p.dt_bias[h]);
+    be_s[lane] = gate_beta(p.b[gi]);
+  }
+  // this tile's value rows of every token, all threads
+  for (int i = tid; i < w * VT; i += Tile::THREADS) {
+    const int t = i / VT, row = tile * VT + i % VT;
+    v_s[i] = row < p.V ? load1(vb + (t0 + t) * p.v_stride + (size_t)h * p.V + row) : 0.f;
   }
   __syncthreads();
 

@@ -21,7 +21,9 @@ class StepBuffers:
         dev = sb.device
         make = (lambda shape: torch.full(shape, fill, dtype=torch.float32, device=dev)) \
             if fill is not None else (lambda shape: torch.empty(shape, dtype=torch.float32, device=dev))
-        self.out = [make((sb.T, sb.HV, sb.V)) for _ in range(sb.L)]
+        # every layer's output in one tensor, so a step's result is one copy
+        self.out_all = make((sb.L, sb.T, sb.HV, sb.V))
+        self.out = list(self.out_all.unbind(0))
         self.rec_u = [make((sb.B, sb.HV, sb.W, sb.V)) for _ in range(sb.L)]
         self.rec_k = [make((sb.B, sb.HV, sb.W, sb.K)) for _ in range(sb.L)]
         self.rec_g = [make((sb.B, sb.HV, sb.W)) for _ in range(sb.L)]
@@ -69,3 +71,43 @@ def native_buffers(sb: SpecBatch, fill: Optional[float] = None):
         out.fill_(fill)
         snaps.fill_(fill)
     return out, snaps
+
+
+def pack_inputs(sb: SpecBatch) -> torch.Tensor:
+    """Move every per-step input of `sb` (q/k/v or the fused projection,
+    a, b and the row metadata of all layers) into one contiguous device
+    byte arena and rebind `sb`'s tensors to views of it, keeping shapes and
+    strides.  A step's inputs can then arrive with a single host-to-device
+    copy.  Returns the arena."""
+    roots = []          # (owner list, index or None, tensor) for tensors owning storage
+    for l in range(sb.L):
+        if sb.fused_qkv:
+            roots.append(("fused_qkv", l, sb.fused_qkv[l]))
+        else:
+            roots += [("q", l, sb.q[l]), ("k", l, sb.k[l]), ("v", l, sb.v[l])]
+        roots += [("a", l, sb.a[l]), ("b", l, sb.b[l])]
+    for name in ("token_start", "window_len", "accepted_len", "slot_table", "seq_pos"):
+        if getattr(sb, name) is not None:
+            roots.append((name, None, getattr(sb, name)))
+    align = 256
+    offsets, total = [], 0
+    for _, _, t in roots:
+        assert t.is_contiguous()
+        offsets.append(total)
+        total += -(-t.numel() * t.element_size() // align) * align
+    arena = torch.empty(total, dtype=torch.uint8, device=sb.device)
+    for (name, l, t), off in zip(roots, offsets):
+        nbytes = t.numel() * t.element_size()
+        view = arena[off:off + nbytes].view(t.dtype).view(t.shape)
+        view.copy_(t)
+        if l is None:
+            setattr(sb, name, view)
+        else:
+            getattr(sb, name)[l] = view
+    if sb.fused_qkv:
+        HK, HV, K, V = sb.HK, sb.HV, sb.K, sb.V
+        for l, buf in enumerate(sb.fused_qkv):
+            sb.q[l] = buf[:, :HK * K].unflatten(1, (HK, K))
+            sb.k[l] = buf[:, HK * K:2 * HK * K].unflatten(1, (HK, K))
+            sb.v[l] = buf[:, 2 * HK * K:].unflatten(1, (HV, V))
+    return arena

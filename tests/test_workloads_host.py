@@ -75,3 +75,22 @@ def test_bench_cpu_baseline_helpers_run_on_cpu():
     bench._oracle_unit_of_work(oracle, d, sb)
     res = bench.cpu_baseline(sb, 0.01)
     assert res["value"] > 0 and res["cores"] >= 1
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_pack_inputs_keeps_values_and_layout(fused):
+    from spec_decode_recurrent_gb300 import step
+    make = wl.long_ragged if fused else wl.all_layer
+    kw = dict(L=2, batch=6, HK=2, HV=4, KV=16, num_slots=12, sentinel=False)
+    if not fused:
+        kw["pad_rows"] = 1
+    sb = make(**kw)
+    ref = {n: [(t.clone(), t.stride()) for t in getattr(sb, n)] for n in ("q", "k", "v", "a", "b")}
+    meta = sb.slot_table.clone()
+    arena = step.pack_inputs(sb)
+    for n, ts in ref.items():
+        for l, (t, stride) in enumerate(ts):
+            got = getattr(sb, n)[l]
+            assert got.shape == t.shape and got.stride() == stride and torch.equal(got, t)
+            assert got.untyped_storage().data_ptr() == arena.untyped_storage().data_ptr()
+    assert torch.equal(sb.slot_table, meta)
