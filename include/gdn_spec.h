@@ -50,7 +50,8 @@
  *     x = seq_pos[r] tokens; seq_pos is read only in align mode.
  *
  * Supported shapes: head_k, head_v in {16, 32, 64, 128}; max_window 1..16;
- * num_v_heads a multiple of num_k_heads; batch, num_layers <= 65535.
+ * num_v_heads a multiple of num_k_heads and <= 65535; batch, num_layers <=
+ * 65535.
  */
 #ifndef GDN_SPEC_H_
 #define GDN_SPEC_H_

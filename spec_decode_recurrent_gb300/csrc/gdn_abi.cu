@@ -18,7 +18,8 @@ size_t dtype_bytes(int d) { return d == GDN_DTYPE_BF16 ? 2 : 4; }
 
 int check_shape(const gdn_shape* s) {
   if (!s) return GDN_ERR_NULL;
-  if (s->num_k_heads < 1 || s->num_v_heads < 1 || s->num_v_heads % s->num_k_heads != 0)
+  if (s->num_k_heads < 1 || s->num_v_heads < 1 || s->num_v_heads % s->num_k_heads != 0 ||
+      s->num_v_heads > 65535)
     return GDN_ERR_UNSUPPORTED;
   if (!supported_width(s->head_k) || !supported_width(s->head_v)) return GDN_ERR_UNSUPPORTED;
   if (s->max_window < 1 || s->max_window > gdn::kMaxWindow) return GDN_ERR_UNSUPPORTED;
@@ -55,9 +56,6 @@ int prepare_verify(gdn::VerifyParams* p, const gdn_shape* s, int32_t batch,
     return GDN_ERR_INVALID;
   if (!aligned(state_pool, 16) || !aligned(out, 4) || !aligned(a, 4) || !aligned(b, 4))
     return GDN_ERR_INVALID;
-  const int vt = gdn::verify_rows_per_cta(s->head_k);
-  if ((int64_t)s->num_v_heads * ((s->head_v + vt - 1) / vt) > 0x7fffffff)
-    return GDN_ERR_UNSUPPORTED;  // grid.x limit
 
   p->HK = s->num_k_heads;
   p->HV = s->num_v_heads;

@@ -164,6 +164,30 @@ __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Four consecutive fp32 state elements as two pairs, bypassing L1.
+__device__ __forceinline__ void load_state_pairs(const float* p, f32x2& a, f32x2& b) {
+  asm("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
+}
+__device__ __forceinline__ void load_state_pairs(const __nv_bfloat16* p, f32x2& a, f32x2& b) {
+  float x[4];
+  load_state4(p, x);
+  a = pack2(x[0], x[1]);
+  b = pack2(x[2], x[3]);
+}
+// Store two pairs as four consecutive state elements (bf16: rounded once).
+__device__ __forceinline__ void store_state_pairs(float* p, f32x2 a, f32x2 b) {
+  asm volatile("st.global.cs.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void store_state_pairs(__nv_bfloat16* p, f32x2 a, f32x2 b) {
+  const float2 x = unpack2(a), y = unpack2(b);
+  const float v[4] = {x.x, x.y, y.x, y.y};
+  store_state4(p, v);
+}
 // The commit's fold on a pair: fma(u, khat, S * alpha) per lane.
 __device__ __forceinline__ f32x2 fold2(f32x2 s, f32x2 alpha, f32x2 u, f32x2 kh) {
   return fma2(u, kh, mul2(s, alpha));

@@ -6,21 +6,27 @@
 // ReplaySSM", Summary and Implementation: a cooperative multi-warp CTA per
 // 128x128 state head; here a head is split into V tiles so that small
 // batches still fill 152 SMs, and a tile is wide enough that the per-token
-// staging -- key/query norms, gates -- is shared by many rows).  Rows of S are independent given (khat, qhat, alpha, beta, v_i),
-// so tiles never communicate; the only reductions are over K, inside a
-// group of K/16 lanes, by warp shuffles.
+// staging -- key/query norms, gates -- is shared by many rows).  Rows of S
+// are independent given (khat, qhat, alpha, beta, v_i), so tiles never
+// communicate; the only reductions are over K, inside a group of K/16
+// lanes, by warp shuffles.
 //
 // Register layout of a tile, for K = 128: LPR = 8 lanes share one state row
 // and each lane holds 16 of its columns, as four 4-column chunks at columns
-// 4 * (l + LPR * m), m = 0..3, so a warp's load of chunk m reads whole
-// 128-byte lines.  A warp covers RPW = 32 / LPR rows per row group and each
-// thread keeps RPT row groups.
+// 4 * (l + LPR * m), m = 0..3, kept as eight packed fp32 pairs; a warp's
+// load of chunk m reads whole 128-byte lines.  A warp covers RPW = 32 / LPR
+// rows per row group and each thread keeps RPT row groups.
+//
+// Per token: H = alpha * S; both dot products are taken in one pass over H,
+// d = H khat and H qhat; then u = beta * (v - d), S = H + u khat^T and
+// o = S qhat evaluated as H qhat + u * (khat . qhat), the same value in
+// exact arithmetic with the output off the state update's critical path.
 //
 // VERIFY mode writes o_t and the replay record (u_t, khat_t, alpha_t) and no
 // state (vLLM PR "[Spec Decode][Qwen4Exp] RecoverSSM for Qwen GDN and the
 // PLE short conv", Purpose).  NATIVE mode writes o_t and the full state after
 // every token instead.  Both run the identical arithmetic, so their outputs
-// agree bit for bit.
+// agree bit for bit, and the state update is the commit's fold.
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
 
@@ -28,32 +34,28 @@ namespace gdn {
 
 template <int K>
 struct VerifyTile {
-  static constexpr int LPR = K / 16;          // lanes per state row
-  static constexpr int RPW = 32 / LPR;        // rows per warp per row group
+  static constexpr int LPR = K / 16;              // lanes per state row
+  static constexpr int RPW = 32 / LPR;            // rows per warp per row group
   static constexpr int RPT = (K == 128) ? 2 : 1;  // row groups per thread
   static constexpr int WARPS = 8;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int VT = WARPS * RPW * RPT;    // state rows per CTA
-  static constexpr int CPL = 16;              // columns per lane
 };
 
 // Dynamic shared memory of one verify CTA, in floats.
 template <int K>
 __host__ __device__ constexpr int verify_smem_floats(int W) {
-  return W * (2 * K + VerifyTile<K>::VT + 2);
+  return W * (2 * K + VerifyTile<K>::VT + 3);
 }
 
-template <int K, typename QKV, typename ST, bool NATIVE>
+template <int K, typename QKV, typename ST, bool NATIVE, bool FULL>
 __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
     gdn_verify_kernel(const VerifyParams p) {
   using Tile = VerifyTile<K>;
   constexpr int LPR = Tile::LPR, RPW = Tile::RPW, RPT = Tile::RPT, VT = Tile::VT;
   extern __shared__ float smem[];
 
-  const int ntiles = (p.V + VT - 1) / VT;
-  const int tile = blockIdx.x % ntiles;
-  const int h = blockIdx.x / ntiles;
-  const int r = blockIdx.y;
+  const int tile = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- row plan: identical checks in every CTA of the row
@@ -72,42 +74,39 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
   }
   if (src.slot < 0) return;  // null row or empty window: writes nothing
 
-  const int group = p.HV / p.HK;
-  const int hk = h / group;
+  const int hk = h / (p.HV / p.HK);
   const int l = lane % LPR;   // column lane inside the row group
   const int lr = lane / LPR;  // row inside the warp's row group
 
   // ---- issue the checkpoint tile loads first; they stay in flight while
-  // ---- the token inputs are staged
+  // ---- the token inputs are staged.  Row group g holds columns
+  // ---- 4*(l + LPR*m) + {0..3}: s[g][2m] = +0,+1 and s[g][2m+1] = +2,+3.
   const ST* S0 = static_cast<const ST*>(p.pool) +
                  ((size_t)src.slot * p.HV + h) * (size_t)p.V * K;
-  // tile row group g holds columns 4*(l + LPR*m) + {0..3}, m = 0..3, as
-  // eight packed pairs: s[g][2m] = columns +0,+1 and s[g][2m+1] = +2,+3
   f32x2 s[RPT][8];
   int rows[RPT];
 #pragma unroll
   for (int g = 0; g < RPT; ++g) {
     rows[g] = tile * VT + (g * Tile::WARPS + warp) * RPW + lr;
-    if (rows[g] < p.V) {
+    if (FULL || rows[g] < p.V) {
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float x[4];
-        load_state4(S0 + (size_t)rows[g] * K + 4 * (l + LPR * m), x);
-        s[g][2 * m] = pack2(x[0], x[1]);
-        s[g][2 * m + 1] = pack2(x[2], x[3]);
-      }
+      for (int m = 0; m < 4; ++m)
+        load_state_pairs(S0 + (size_t)rows[g] * K + 4 * (l + LPR * m), s[g][2 * m],
+                         s[g][2 * m + 1]);
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) s[g][j] = 0ull;
     }
   }
 
-  // ---- stage normalised keys / queries, values and gates in shared memory
+  // ---- stage normalised keys / queries, their dot product, values and
+  // ---- gates of the whole window in shared memory
   float* kh_s = smem;                   // [W][K]
   float* qh_s = kh_s + p.W * K;         // [W][K]
   float* v_s = qh_s + p.W * K;          // [W][VT]
   float* al_s = v_s + p.W * VT;         // [W]
   float* be_s = al_s + p.W;             // [W]
+  float* kq_s = be_s + p.W;             // [W]
   const QKV* qb = static_cast<const QKV*>(p.q);
   const QKV* kb = static_cast<const QKV*>(p.k);
   const QKV* vb = static_cast<const QKV*>(p.v);
@@ -132,14 +131,22 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
     // x / sqrt(|x|^2 + eps) as x * rsqrt(|x|^2 + eps), rsqrt correctly rounded
     const float kr = __frsqrt_rn(__fadd_rn(ks, kL2NormEps));
     const float qr = __frsqrt_rn(__fadd_rn(qs, kL2NormEps));
-    if (lane < K / 4) {
-      *reinterpret_cast<float4*>(kh_s + t * K + 4 * lane) =
-          make_float4(__fmul_rn(kx[0], kr), __fmul_rn(kx[1], kr), __fmul_rn(kx[2], kr),
-                      __fmul_rn(kx[3], kr));
-      *reinterpret_cast<float4*>(qh_s + t * K + 4 * lane) =
-          make_float4(__fmul_rn(qx[0], qr), __fmul_rn(qx[1], qr), __fmul_rn(qx[2], qr),
-                      __fmul_rn(qx[3], qr));
+    float kn[4], qn[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      kn[e] = __fmul_rn(kx[e], kr);
+      qn[e] = __fmul_rn(qx[e], qr);
     }
+    float kq = __fmul_rn(kn[0], qn[0]);
+#pragma unroll
+    for (int e = 1; e < 4; ++e) kq = __fmaf_rn(kn[e], qn[e], kq);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) kq = __fadd_rn(kq, __shfl_xor_sync(0xffffffffu, kq, off));
+    if (lane < K / 4) {
+      *reinterpret_cast<float4*>(kh_s + t * K + 4 * lane) = make_float4(kn[0], kn[1], kn[2], kn[3]);
+      *reinterpret_cast<float4*>(qh_s + t * K + 4 * lane) = make_float4(qn[0], qn[1], qn[2], qn[3]);
+    }
+    if (lane == 0) kq_s[t] = kq;
   }
   // gates of the whole window: one lane per token in the last warp
   if (warp == Tile::WARPS - 1 && lane < w) {
@@ -150,20 +157,34 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
   // this tile's value rows of every token, all threads
   for (int i = tid; i < w * VT; i += Tile::THREADS) {
     const int t = i / VT, row = tile * VT + i % VT;
-    v_s[i] = row < p.V ? load1(vb + (t0 + t) * p.v_stride + (size_t)h * p.V + row) : 0.f;
+    v_s[i] = (FULL || row < p.V) ? load1(vb + (t0 + t) * p.v_stride + (size_t)h * p.V + row) : 0.f;
   }
   __syncthreads();
 
   const size_t rec_base = ((size_t)r * p.HV + h) * p.W;  // record position 0
   if (!NATIVE && tile == 0) {
-    for (int i = tid; i < w * K; i += Tile::THREADS)
-      p.rec_k[rec_base * K + i] = kh_s[i];
+    for (int i = tid; i < w * K; i += Tile::THREADS) p.rec_k[rec_base * K + i] = kh_s[i];
     if (tid < w) p.rec_g[rec_base + tid] = al_s[tid];
   }
 
+  // ---- output / record / snapshot cursors, advanced once per token
+  const bool writer = (l == 0);
+  float* optr[RPT];
+  float* uptr[RPT];
+  ST* sptr[RPT];
+#pragma unroll
+  for (int g = 0; g < RPT; ++g) {
+    optr[g] = p.out + t0 * p.out_stride + (size_t)h * p.V + rows[g];
+    uptr[g] = NATIVE ? nullptr : p.rec_u + rec_base * p.V + rows[g];
+    sptr[g] = NATIVE ? static_cast<ST*>(p.snaps) + ((size_t)r * p.W * p.HV + h) * (size_t)p.V * K +
+                           (size_t)rows[g] * K + 4 * l
+                     : nullptr;
+  }
+  const size_t snap_step = (size_t)p.HV * p.V * K;
+
   // ---- the draft window, token by token, state in registers
   for (int t = 0; t < w; ++t) {
-    const float be = be_s[t];
+    const float be = be_s[t], kq = kq_s[t];
     const f32x2 al2 = pack2(al_s[t], al_s[t]);
     f32x2 kk[8], qq[8];
 #pragma unroll
@@ -173,62 +194,51 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
       kk[2 * m] = k4.x; kk[2 * m + 1] = k4.y;
       qq[2 * m] = q4.x; qq[2 * m + 1] = q4.y;
     }
-    const long long orow = t0 + t;
 #pragma unroll
     for (int g = 0; g < RPT; ++g) {
       // H = alpha * S
 #pragma unroll
       for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], al2);
-      // d = H khat: two pair accumulators (pairs 0-3, 4-7), their four
-      // lanes summed in a fixed order, then the LPR lanes of the row
+      // d = H khat and H qhat in one pass: pair accumulators over pairs
+      // 0-3 and 4-7, combined pairwise, lanes summed, then the LPR lanes
       f32x2 da = mul2(s[g][0], kk[0]), db = mul2(s[g][4], kk[4]);
+      f32x2 oa = mul2(s[g][0], qq[0]), ob = mul2(s[g][4], qq[4]);
 #pragma unroll
       for (int j = 1; j < 4; ++j) {
         da = fma2(s[g][j], kk[j], da);
         db = fma2(s[g][4 + j], kk[4 + j], db);
+        oa = fma2(s[g][j], qq[j], oa);
+        ob = fma2(s[g][4 + j], qq[4 + j], ob);
       }
-      const float2 fa = unpack2(da), fb = unpack2(db);
-      float d = __fadd_rn(__fadd_rn(fa.x, fa.y), __fadd_rn(fb.x, fb.y));
+      const float2 dd = unpack2(add2(da, db)), oo = unpack2(add2(oa, ob));
+      float d = __fadd_rn(dd.x, dd.y), o = __fadd_rn(oo.x, oo.y);
 #pragma unroll
-      for (int off = LPR / 2; off >= 1; off >>= 1)
+      for (int off = LPR / 2; off >= 1; off >>= 1) {
         d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, off));
-      const int row_local = rows[g] - tile * VT;
-      const float vi = rows[g] < p.V ? v_s[t * VT + row_local] : 0.f;
+        o = __fadd_rn(o, __shfl_xor_sync(0xffffffffu, o, off));
+      }
+      const float vi = (FULL || rows[g] < p.V) ? v_s[t * VT + rows[g] - tile * VT] : 0.f;
       const float u = __fmul_rn(be, __fsub_rn(vi, d));
+      o = __fmaf_rn(u, kq, o);
       // S = H + u khat^T
       const f32x2 u2 = pack2(u, u);
 #pragma unroll
       for (int j = 0; j < 8; ++j) s[g][j] = fma2(u2, kk[j], s[g][j]);
-      // o = S qhat
-      f32x2 oa = mul2(s[g][0], qq[0]), ob = mul2(s[g][4], qq[4]);
-#pragma unroll
-      for (int j = 1; j < 4; ++j) {
-        oa = fma2(s[g][j], qq[j], oa);
-        ob = fma2(s[g][4 + j], qq[4 + j], ob);
-      }
-      const float2 ga = unpack2(oa), gb = unpack2(ob);
-      float o = __fadd_rn(__fadd_rn(ga.x, ga.y), __fadd_rn(gb.x, gb.y));
-#pragma unroll
-      for (int off = LPR / 2; off >= 1; off >>= 1)
-        o = __fadd_rn(o, __shfl_xor_sync(0xffffffffu, o, off));
 
-      if (rows[g] < p.V) {
-        if (l == 0) {
-          p.out[orow * p.out_stride + (size_t)h * p.V + rows[g]] = o;
-          if (!NATIVE) p.rec_u[(rec_base + t) * p.V + rows[g]] = u;
+      if (FULL || rows[g] < p.V) {
+        if (writer) {
+          *optr[g] = o;
+          if (!NATIVE) *uptr[g] = u;
         }
         if (NATIVE) {
-          ST* snap = static_cast<ST*>(p.snaps) +
-                     (((size_t)r * p.W + t) * p.HV + h) * (size_t)p.V * K +
-                     (size_t)rows[g] * K;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const float2 a = unpack2(s[g][2 * m]), b = unpack2(s[g][2 * m + 1]);
-            const float x[4] = {a.x, a.y, b.x, b.y};
-            store_state4(snap + 4 * (l + LPR * m), x);
-          }
+          for (int m = 0; m < 4; ++m)
+            store_state_pairs(sptr[g] + 4 * LPR * m, s[g][2 * m], s[g][2 * m + 1]);
         }
       }
+      optr[g] += p.out_stride;
+      if (!NATIVE) uptr[g] += p.V;
+      if (NATIVE) sptr[g] += snap_step;
     }
   }
 }
@@ -237,9 +247,12 @@ template <int K, typename QKV, typename ST, bool NATIVE>
 static int launch_one(const VerifyParams& p, cudaStream_t stream) {
   using Tile = VerifyTile<K>;
   const int ntiles = (p.V + Tile::VT - 1) / Tile::VT;
-  dim3 grid(ntiles * p.HV, p.batch);
+  dim3 grid(ntiles, p.HV, p.batch);
   const size_t smem = sizeof(float) * verify_smem_floats<K>(p.W);
-  gdn_verify_kernel<K, QKV, ST, NATIVE><<<grid, Tile::THREADS, smem, stream>>>(p);
+  if (p.V % Tile::VT == 0)
+    gdn_verify_kernel<K, QKV, ST, NATIVE, true><<<grid, Tile::THREADS, smem, stream>>>(p);
+  else
+    gdn_verify_kernel<K, QKV, ST, NATIVE, false><<<grid, Tile::THREADS, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
