@@ -81,6 +81,8 @@ extern "C" {
                                  /* or holds -1 although the row is live             */
 #define GDN_ROW_ERR_SEQPOS 16    /* align mode: seq_pos < 1 on a live row             */
 #define GDN_ROW_ERR_TOKENS 32    /* token rows outside [0, num_tokens)                */
+#define GDN_ROW_ERR_GROUP 64     /* grouped commit: a layer's group id is outside     */
+                                 /* [0, num_groups); that layer writes nothing       */
 
 typedef struct gdn_shape {
   int32_t num_k_heads; /* HK                                              */
@@ -163,6 +165,35 @@ int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers,
                       const int32_t* slot_table, int32_t slot_table_stride,
                       const int32_t* seq_pos, int32_t block_size, int32_t* err,
                       void* stream);
+
+/*
+ * Grouped all-layer commit: one launch covering every KV-cache group, for
+ * engines whose GDN layers are split into groups with their own state
+ * indices (vLLM PR above, review thread: a grouped commit over a
+ * [group, batch] state-index table instead of one commit per group).
+ *
+ *   num_groups     >= 1
+ *   layer_group    device int32 [num_layers]: group of each layer.
+ *   slot_tables    device int32 [num_groups][batch][slot_table_stride];
+ *                  group g's table starts group_stride elements after
+ *                  group g-1's (group_stride >= batch * slot_table_stride).
+ * Everything else as gdn_replay_commit, whose semantics each layer follows
+ * with its group's table.  Row errors are OR-ed over all groups; a layer
+ * with an out-of-range group id writes nothing and sets GDN_ROW_ERR_GROUP.
+ */
+int gdn_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers,
+                              int32_t num_groups, const int32_t* layer_group,
+                              int32_t batch, int32_t num_slots,
+                              void* const* state_pools,
+                              const float* const* rec_u,
+                              const float* const* rec_k,
+                              const float* const* rec_g,
+                              const int32_t* window_len,
+                              const int32_t* accepted_len,
+                              const int32_t* slot_tables,
+                              int32_t slot_table_stride, int64_t group_stride,
+                              const int32_t* seq_pos, int32_t block_size,
+                              int32_t* err, void* stream);
 
 /*
  * Native baseline of one layer: the verify's recurrence with the full

@@ -77,6 +77,9 @@ def _load():
             lib.gdn_oracle_replay_commit.restype = _i
             lib.gdn_oracle_replay_commit.argtypes = (
                 [_i] * 7 + [_D] * 5 + [_I, _I, _I, _i, _I, _i, _I])
+            lib.gdn_oracle_replay_commit_grouped.restype = _i
+            lib.gdn_oracle_replay_commit_grouped.argtypes = (
+                [_i] * 7 + [_D] * 5 + [_I, _I, _I, _i, ctypes.c_long, _I, _i, _I, _i, _I])
             lib.gdn_oracle_num_threads.restype = _i
             lib.gdn_oracle_num_threads.argtypes = []
             _lib = lib
@@ -235,11 +238,13 @@ def spec_verify(*, q, k, v, a, b, A_log, dt_bias, token_start, window_len, pool,
 
 
 def replay_commit(*, pools, rec_u, rec_k, rec_g, window_len, accepted_len, slot_table,
-                  seq_pos=None, block_size=0, max_window):
+                  seq_pos=None, block_size=0, max_window, layer_group=None):
     """All-layer commit from records.
 
     pools [L, num_slots, HV, V, K]; rec_u [L, B, HV, W, V]; rec_k [L, B, HV, W, K];
-    rec_g [L, B, HV, W].  Returns (new_pools float64, row_err).
+    rec_g [L, B, HV, W].  slot_table [B, stride], or [G, B, stride] with
+    layer_group [L] naming each layer's group.  Returns (new_pools float64,
+    row_err).
     """
     pools_in = _f64(pools)
     pools_out = pools_in.copy()
@@ -248,14 +253,19 @@ def replay_commit(*, pools, rec_u, rec_k, rec_g, window_len, accepted_len, slot_
     slot_table = _i32(slot_table)
     if slot_table.ndim == 1:
         slot_table = slot_table.reshape(-1, 1)
+    if slot_table.ndim == 2:
+        slot_table = slot_table[None]
+    G = slot_table.shape[0]
+    lg = None if layer_group is None else _i32(layer_group)
     L, num_slots, HV, V, K = pools_in.shape
     B = window_len.shape[0]
     sp = None if seq_pos is None else _i32(seq_pos)
     row_err = np.zeros(B, dtype=np.int32)
-    rc = _load().gdn_oracle_replay_commit(
+    rc = _load().gdn_oracle_replay_commit_grouped(
         L, HV, K, V, int(max_window), B, num_slots, _dp(pools_in), _dp(pools_out),
         _dp(rec_u), _dp(rec_k), _dp(rec_g), _ip(window_len), _ip(accepted_len),
-        _ip(slot_table), slot_table.shape[1], _ip(sp), int(block_size), _ip(row_err))
+        _ip(lg), G, slot_table.shape[1] * slot_table.shape[2], _ip(slot_table),
+        slot_table.shape[2], _ip(sp), int(block_size), _ip(row_err))
     if rc != 0:
         raise ValueError(f"oracle replay_commit rejected the shape ({rc})")
     return pools_out, row_err

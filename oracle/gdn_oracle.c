@@ -312,7 +312,7 @@ int gdn_oracle_spec_verify(int HK, int HV, int K, int V, int W_max, int B,
   return 0;
 }
 
-/* All-layer replay commit from records.
+/* All-layer replay commit from records, with layers in KV-cache groups.
  *   pools_in  [L][num_slots][HV][V][K]  states before the commit (read only)
  *   pools_out [L][num_slots][HV][V][K]  the caller's copy of pools_in; the
  *             planned slots are overwritten.  Reading every fold's source
@@ -321,38 +321,52 @@ int gdn_oracle_spec_verify(int HK, int HV, int K, int V, int W_max, int B,
  *             guarantees on the GPU (vLLM PR above, Commits item 6).
  *   rec_u [L][B][HV][W_max][V], rec_k [L][B][HV][W_max][K],
  *   rec_g [L][B][HV][W_max]
- *   row_err[B] receives the row's error bits. */
-int gdn_oracle_replay_commit(int L, int HV, int K, int V, int W_max, int B,
-                             int num_slots, const double* pools_in,
-                             double* pools_out, const double* rec_u,
-                             const double* rec_k, const double* rec_g,
-                             const int32_t* window_len,
-                             const int32_t* accepted_len,
-                             const int32_t* slot_table, int table_stride,
-                             const int32_t* seq_pos, int block_size,
-                             int32_t* row_err) {
-  if (L <= 0 || HV <= 0 || K <= 0 || V <= 0 || W_max <= 0) return -2;
+ *   layer_group [L]: group of each layer (NULL: every layer in group 0);
+ *   group g's slot table starts at slot_table + g * group_stride (the
+ *   [group, batch] state-index table of the vLLM PR's review thread).
+ *   row_err[B] receives the row's error bits, OR-ed over the groups. */
+int gdn_oracle_replay_commit_grouped(int L, int HV, int K, int V, int W_max,
+                                     int B, int num_slots,
+                                     const double* pools_in, double* pools_out,
+                                     const double* rec_u, const double* rec_k,
+                                     const double* rec_g,
+                                     const int32_t* window_len,
+                                     const int32_t* accepted_len,
+                                     const int32_t* layer_group,
+                                     int num_groups, long group_stride,
+                                     const int32_t* slot_table,
+                                     int table_stride, const int32_t* seq_pos,
+                                     int block_size, int32_t* row_err) {
+  if (L <= 0 || HV <= 0 || K <= 0 || V <= 0 || W_max <= 0 || num_groups <= 0)
+    return -2;
+  if (layer_group)
+    for (int l = 0; l < L; ++l)
+      if (layer_group[l] < 0 || layer_group[l] >= num_groups) return -3;
   size_t VK = (size_t)V * K;
   size_t pool_elems = (size_t)num_slots * HV * VK;
   int max_writes = 2 + W_max;
-  for (int r = 0; r < B; ++r) {
-    int32_t src, slots[64], ntok[64];
-    int sp = seq_pos ? seq_pos[r] : 0;
-    int nw = gdn_oracle_commit_plan(window_len[r], accepted_len[r],
-                                    slot_table + (size_t)r * table_stride,
-                                    table_stride, sp, block_size, num_slots,
-                                    W_max, &src, slots, ntok, max_writes);
-    row_err[r] = nw < 0 ? -nw - 1 : 0;
+  for (int r = 0; r < B; ++r) row_err[r] = 0;
+  for (int g = 0; g < num_groups; ++g) {
+    for (int r = 0; r < B; ++r) {
+      int32_t src, slots[64], ntok[64];
+      int sp = seq_pos ? seq_pos[r] : 0;
+      const int32_t* trow = slot_table + g * group_stride + (size_t)r * table_stride;
+      int nw = gdn_oracle_commit_plan(window_len[r], accepted_len[r], trow,
+                                      table_stride, sp, block_size, num_slots,
+                                      W_max, &src, slots, ntok, max_writes);
+      if (nw < 0) row_err[r] |= -nw - 1;
+    }
   }
 #pragma omp parallel for schedule(dynamic, 1)
   for (long unit = 0; unit < (long)L * B * HV; ++unit) {
     int l = (int)(unit / ((long)B * HV));
     int r = (int)((unit / HV) % B);
     int h = (int)(unit % HV);
+    int g = layer_group ? layer_group[l] : 0;
     int32_t src, slots[64], ntok[64];
     int sp = seq_pos ? seq_pos[r] : 0;
-    int nw = gdn_oracle_commit_plan(window_len[r], accepted_len[r],
-                                    slot_table + (size_t)r * table_stride,
+    const int32_t* trow = slot_table + g * group_stride + (size_t)r * table_stride;
+    int nw = gdn_oracle_commit_plan(window_len[r], accepted_len[r], trow,
                                     table_stride, sp, block_size, num_slots,
                                     W_max, &src, slots, ntok, max_writes);
     if (nw <= 0) continue;
@@ -369,4 +383,20 @@ int gdn_oracle_replay_commit(int L, int HV, int K, int V, int W_max, int B,
     free(S);
   }
   return 0;
+}
+
+/* All-layer replay commit with every layer reading the same slot table. */
+int gdn_oracle_replay_commit(int L, int HV, int K, int V, int W_max, int B,
+                             int num_slots, const double* pools_in,
+                             double* pools_out, const double* rec_u,
+                             const double* rec_k, const double* rec_g,
+                             const int32_t* window_len,
+                             const int32_t* accepted_len,
+                             const int32_t* slot_table, int table_stride,
+                             const int32_t* seq_pos, int block_size,
+                             int32_t* row_err) {
+  return gdn_oracle_replay_commit_grouped(
+      L, HV, K, V, W_max, B, num_slots, pools_in, pools_out, rec_u, rec_k,
+      rec_g, window_len, accepted_len, NULL, 1, 0, slot_table, table_stride,
+      seq_pos, block_size, row_err);
 }

@@ -20,7 +20,9 @@ from . import build as _build
 GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
 ROW_ERR_WINDOW, ROW_ERR_ACCEPTED, ROW_ERR_SLOT = 1, 2, 4
 ROW_ERR_BLOCK, ROW_ERR_SEQPOS, ROW_ERR_TOKENS = 8, 16, 32
-ENTRY_POINTS = ("gdn_spec_verify", "gdn_replay_commit", "gdn_native_spec_snapshot")
+ROW_ERR_GROUP = 64
+ENTRY_POINTS = ("gdn_spec_verify", "gdn_replay_commit", "gdn_replay_commit_grouped",
+                "gdn_native_spec_snapshot")
 
 _ERRORS = {-1: "null pointer", -2: "unsupported shape or dtype",
            -3: "invalid count, stride, alignment or block size", -4: "CUDA launch failed"}
@@ -68,6 +70,10 @@ def load() -> ctypes.CDLL:
             lib.gdn_replay_commit.argtypes = [ctypes.POINTER(gdn_shape), _I32, _I32, _I32,
                                               _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32,
                                               _P, _P]
+            lib.gdn_replay_commit_grouped.restype = ctypes.c_int
+            lib.gdn_replay_commit_grouped.argtypes = [
+                ctypes.POINTER(gdn_shape), _I32, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                _P, _I32, _I64, _P, _I32, _P, _P]
             _lib = lib
     return _lib
 
@@ -231,3 +237,33 @@ def gdn_replay_commit(*, table: LayerTable, num_k_heads: int, window_len, accept
         int(block_size), _ptr(err), _stream(stream))
     if rc != 0:
         raise GDNError("gdn_replay_commit", rc)
+
+
+def gdn_replay_commit_grouped(*, table: LayerTable, num_k_heads: int, layer_group, window_len,
+                              accepted_len, slot_tables, seq_pos=None, block_size=0, err=None,
+                              stream=None) -> None:
+    """All-layer commit in one launch for layers split into KV-cache groups:
+    layer l uses slot_tables[layer_group[l]] ([groups, batch, stride])."""
+    B = window_len.shape[0]
+    _need(B == table.B, "batch must match the record buffers")
+    for name, t in (("window_len", window_len), ("accepted_len", accepted_len)):
+        _contig(t, name, torch.int32)
+        _need(t.shape == (B,), f"{name} must be [batch]")
+    _contig(layer_group, "layer_group", torch.int32)
+    _need(layer_group.shape == (table.num_layers,), "layer_group must be [num_layers]")
+    _contig(slot_tables, "slot_tables", torch.int32)
+    _need(slot_tables.dim() == 3 and slot_tables.shape[1] == B, "slot_tables must be [groups, batch, stride]")
+    if block_size:
+        _contig(seq_pos, "seq_pos", torch.int32)
+    if err is not None:
+        _contig(err, "err", torch.int32)
+    G, _, stride = slot_tables.shape
+    shape = gdn_shape(int(num_k_heads), table.HV, table.K, table.V, table.W, GDN_DTYPE_F32,
+                      _dtype_code(table.state_dtype))
+    rc = load().gdn_replay_commit_grouped(
+        ctypes.byref(shape), table.num_layers, G, _ptr(layer_group), B, table.num_slots,
+        _ptr(table.d_pools), _ptr(table.d_rec_u), _ptr(table.d_rec_k), _ptr(table.d_rec_g),
+        _ptr(window_len), _ptr(accepted_len), _ptr(slot_tables), stride, B * stride,
+        _ptr(seq_pos if block_size else None), int(block_size), _ptr(err), _stream(stream))
+    if rc != 0:
+        raise GDNError("gdn_replay_commit_grouped", rc)

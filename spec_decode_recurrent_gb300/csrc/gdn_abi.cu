@@ -148,22 +148,26 @@ int gdn_native_spec_snapshot(
                             static_cast<cudaStream_t>(stream));
 }
 
-int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
-                      int32_t num_slots, void* const* state_pools, const float* const* rec_u,
-                      const float* const* rec_k, const float* const* rec_g,
-                      const int32_t* window_len, const int32_t* accepted_len,
-                      const int32_t* slot_table, int32_t slot_table_stride,
-                      const int32_t* seq_pos, int32_t block_size, int32_t* err,
-                      void* stream) {
+int gdn_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers, int32_t num_groups,
+                              const int32_t* layer_group, int32_t batch, int32_t num_slots,
+                              void* const* state_pools, const float* const* rec_u,
+                              const float* const* rec_k, const float* const* rec_g,
+                              const int32_t* window_len, const int32_t* accepted_len,
+                              const int32_t* slot_tables, int32_t slot_table_stride,
+                              int64_t group_stride, const int32_t* seq_pos, int32_t block_size,
+                              int32_t* err, void* stream) {
   int rc = check_shape(shape);
   if (rc != GDN_OK || batch == 0) return rc;
-  if (!state_pools || !rec_u || !rec_k || !rec_g || !window_len || !accepted_len || !slot_table)
+  if (!state_pools || !rec_u || !rec_k || !rec_g || !window_len || !accepted_len ||
+      !slot_tables)
     return GDN_ERR_NULL;
+  if (num_groups > 1 && !layer_group) return GDN_ERR_NULL;
   if (block_size < 0 || slot_table_stride < 1) return GDN_ERR_INVALID;
   if (block_size > 0 && !seq_pos) return GDN_ERR_NULL;
-  if (num_layers < 1 || num_layers > 65535 || batch < 0 || batch > 65535 || num_slots < 0)
+  if (num_layers < 1 || num_layers > 65535 || batch < 0 || batch > 65535 || num_slots < 0 ||
+      num_groups < 1)
     return GDN_ERR_INVALID;
-  if (batch == 0) return GDN_OK;
+  if (num_groups > 1 && group_stride < (int64_t)batch * slot_table_stride) return GDN_ERR_INVALID;
   gdn::CommitParams p;
   p.HV = shape->num_v_heads;
   p.V = shape->head_v;
@@ -171,19 +175,34 @@ int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
   p.num_layers = num_layers;
   p.batch = batch;
   p.num_slots = num_slots;
+  p.layer_group = layer_group;
+  p.num_groups = num_groups;
+  p.group_stride = num_groups > 1 ? group_stride : 0;
   p.pools = state_pools;
   p.rec_u = rec_u;
   p.rec_k = rec_k;
   p.rec_g = rec_g;
   p.window_len = window_len;
   p.accepted_len = accepted_len;
-  p.slot_table = slot_table;
+  p.slot_table = slot_tables;
   p.table_stride = slot_table_stride;
   p.seq_pos = seq_pos;
   p.block_size = block_size;
   p.err = err;
   return gdn::launch_commit(p, shape->head_k, shape->state_dtype,
                             static_cast<cudaStream_t>(stream));
+}
+
+int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
+                      int32_t num_slots, void* const* state_pools, const float* const* rec_u,
+                      const float* const* rec_k, const float* const* rec_g,
+                      const int32_t* window_len, const int32_t* accepted_len,
+                      const int32_t* slot_table, int32_t slot_table_stride,
+                      const int32_t* seq_pos, int32_t block_size, int32_t* err,
+                      void* stream) {
+  return gdn_replay_commit_grouped(shape, num_layers, 1, nullptr, batch, num_slots, state_pools,
+                                   rec_u, rec_k, rec_g, window_len, accepted_len, slot_table,
+                                   slot_table_stride, 0, seq_pos, block_size, err, stream);
 }
 
 }  // extern "C"

@@ -1,84 +1,23 @@
-// gdn_async.cuh -- inline-PTX wrappers for the asynchronous copy engine
-// (cp.async.bulk, TMA's untiled form) and shared-memory mbarriers, as used
-// by the pipelined all-layer commit.  Every wait is bounded (by wall time
-// and, as a backstop, by a poll count): it gives up and reports failure, so
-// a kernel can set an error flag and return instead of hanging.
+// gdn_async.cuh -- inline-PTX wrappers for per-thread asynchronous copies
+// global -> shared (cp.async).  A thread issues its copies, keeps working
+// (e.g. issues its own state loads), and later waits for them with a
+// hardware wait (cp.async.wait_all): no polling, so no wait can spin.
 #pragma once
 
 #include <stdint.h>
 
 namespace gdn {
 
-// A wait gives up after kWaitLimitNs of wall time (measured with the
-// global timer): far beyond any legitimate wait in these kernels, short
-// enough to end a broken launch.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kErrTimeout = 1 << 30;  // kernel-level bit in the error word
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-               : "memory");
-}
-
-// Make barrier initialisation visible to the async proxy before first use.
-__device__ __forceinline__ void mbar_fence_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
-                   smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(addr), "r"(parity), "r"(1000u)
-      : "memory");
-  return done != 0;
-}
-
-// Wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t addr = smem_addr(bar);
-  if (mbar_try_wait(addr, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (uint32_t round = 0; round < (1u << 20); ++round) {
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(addr, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
-  return false;
-}
-
-// Per-thread asynchronous copies global -> shared (cp.async): 16 bytes
-// (L2 only) or 4 bytes, committed as one group and awaited with a
-// hardware wait (no polling).
+// 16 bytes, cached in L2 only; both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
 }
+// 4 bytes; both addresses 4-byte aligned.
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
@@ -88,17 +27,6 @@ __device__ __forceinline__ void cp_async_commit() {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-// Bulk copy global -> shared, completion counted in bytes on `bar`.
-// Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
 }
 
 }  // namespace gdn

@@ -21,11 +21,9 @@
 // therefore never read after it has been overwritten, which is the
 // guarantee "final folds before boundary folds" gives in a split commit.
 //
-// Two schedules are built: a one-CTA-per-tile kernel (gdn_commit_kernel)
-// and a persistent, pipelined kernel (gdn_commit_pipelined_kernel) that
-// streams heads through shared memory with bulk asynchronous copies.
-#include <stdlib.h>
-
+// One CTA per (layer, row, head, 64-row tile): the record of the accepted
+// tokens is staged with per-thread asynchronous copies (cp.async) issued
+// ahead of the tile's loads, so four CTAs per SM keep ~128 KiB in flight.
 #include "gdn_async.cuh"
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
@@ -43,11 +41,21 @@ struct RowCommit {
   long long p0;  // tokens already in the checkpoint (align mode)
 };
 
-__device__ __forceinline__ RowCommit commit_row_plan(const CommitParams& p, int r) {
+// Slot-table row of request r for the group of `layer`, or NULL when the
+// layer's group id is outside [0, num_groups).
+__device__ __forceinline__ const int32_t* group_table_row(const CommitParams& p, int layer,
+                                                          int r) {
+  const int g = p.layer_group ? p.layer_group[layer] : 0;
+  if (g < 0 || g >= p.num_groups) return nullptr;
+  return p.slot_table + g * p.group_stride + (size_t)r * p.table_stride;
+}
+
+__device__ __forceinline__ RowCommit commit_row_plan(const CommitParams& p, int r,
+                                                     const int32_t* trow) {
   RowCommit c{0, false, -1, -1, 0, 0};
+  if (trow == nullptr) { c.err = GDN_ROW_ERR_GROUP; return c; }
   const int w = p.window_len[r];
   const int n = p.accepted_len[r];
-  const int32_t* trow = p.slot_table + (size_t)r * p.table_stride;
   SourceSlot src = source_slot(w, p.W, trow, p.table_stride, p.block_size, p.seq_pos, r,
                                p.num_slots);
   if (src.err) { c.err = src.err; return c; }
@@ -176,9 +184,10 @@ __global__ void __launch_bounds__(kCommitThreads)
   const int r = blockIdx.y, layer = blockIdx.z;
   const int tid = threadIdx.x;
 
-  const RowCommit plan = commit_row_plan(p, r);
+  const int32_t* trow = group_table_row(p, layer, r);
+  const RowCommit plan = commit_row_plan(p, r, trow);
   if (plan.err) {
-    if (p.err && tid == 0 && tile == 0 && h == 0 && layer == 0) atomicOr(p.err, plan.err);
+    if (p.err && tid == 0 && tile == 0 && h == 0) atomicOr(p.err, plan.err);
     return;
   }
   if (!plan.live) return;  // null row or nothing accepted
@@ -219,7 +228,6 @@ __global__ void __launch_bounds__(kCommitThreads)
   __syncthreads();
 
   const int col = (tid % CPR) * E;  // fixed column block of this thread
-  const int32_t* trow = p.slot_table + (size_t)r * p.table_stride;
   for (int t = 0; t < n; ++t) {
     fold_token<K, ST, M, NT>(x, g_s[t], k_s, u_s, t, TILE_ROWS, col, c0, row_base, nchunks);
     // align mode: the state after token p lands in slot(p) when p closes a block
@@ -232,192 +240,7 @@ __global__ void __launch_bounds__(kCommitThreads)
   store_chunks<ST, M, NT>(pool + ((size_t)plan.fin * p.HV + h) * head, x, c0, nchunks);
 }
 
-// ---------------------------------------------------------------------------
-// Pipelined form: a persistent CTA per SM streams heads through a ring of
-// shared-memory stages.  Warp 0 (one elected lane) is the producer: it walks
-// the CTA's (layer, row) pairs, evaluates each row's plan once, and for every
-// value head waits for a free stage, writes a small ticket (accepted length,
-// slots, gates) into it and issues bulk asynchronous copies (cp.async.bulk,
-// TMA's untiled form) of the checkpoint head and of the accepted tokens'
-// record, completing on the stage's "full" mbarrier.  Warps 1..8 are
-// consumers: they wait for a stage, read the ticket, pull their chunks into
-// registers, fold, release the stage and store from registers.  A ticket
-// with n < 0 ends the work.
-constexpr int kConsumerWarps = 8;
-constexpr int kPipeThreads = 32 * (kConsumerWarps + 1);
-constexpr int kMaxStages = 4;
-
-struct StageTicket {
-  int n;  // accepted tokens; < 0 ends the work
-  int layer, row, head;
-  int fin;  // final slot
-  int pad;
-  long long p0;  // checkpoint position (align mode)
-  float alpha[kMaxWindow];
-};
-
-template <int K, typename ST>
-__global__ void __launch_bounds__(kPipeThreads, 1)
-    gdn_commit_pipelined_kernel(const CommitParams p, int num_stages) {
-  using C = Chunk<ST>;
-  constexpr int E = C::E;
-  constexpr int CPR = K / E;
-  constexpr int NT = kConsumerWarps * 32;
-  constexpr int MAXM = (128 * K) / E / NT;
-  constexpr int M = MAXM > 0 ? MAXM : 1;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-
-  const int V = p.V;
-  const uint32_t state_bytes = (uint32_t)(V * K * sizeof(ST));
-  const uint32_t u_bytes = (uint32_t)(p.W * V * 4), k_bytes = (uint32_t)(p.W * K * 4);
-  const uint32_t stage_bytes = state_bytes + u_bytes + k_bytes;
-  StageTicket* tickets =
-      reinterpret_cast<StageTicket*>(smem_raw + (size_t)num_stages * stage_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(tickets + kMaxStages);
-  uint64_t* empty = full + kMaxStages;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < num_stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    mbar_fence_init();
-  }
-  __syncthreads();
-
-  const size_t head = (size_t)V * K;
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane != 0) return;
-    uint32_t it = 0;
-    bool ok = true;
-    const long long pairs = (long long)p.num_layers * p.batch;
-    for (long long q = blockIdx.x; q < pairs && ok; q += gridDim.x) {
-      const int layer = (int)(q / p.batch), r = (int)(q % p.batch);
-      const RowCommit plan = commit_row_plan(p, r);
-      if (plan.err) {
-        if (p.err && layer == 0) atomicOr(p.err, plan.err);
-        continue;
-      }
-      if (!plan.live) continue;
-      const size_t rec0 = (size_t)r * p.HV * p.W;
-      const ST* pool = static_cast<const ST*>(p.pools[layer]);
-      const float* ru = p.rec_u[layer];
-      const float* rk = p.rec_k[layer];
-      const float* rg = p.rec_g[layer];
-      for (int h = 0; h < p.HV; ++h) {
-        const int s = (int)(it % (uint32_t)num_stages);
-        const uint32_t round = it / (uint32_t)num_stages;
-        if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u)) {
-          if (p.err) atomicOr(p.err, kErrTimeout);
-          ok = false;
-          break;
-        }
-        StageTicket& tk = tickets[s];
-        const size_t rec = rec0 + (size_t)h * p.W;
-        tk.n = plan.n;
-        tk.layer = layer;
-        tk.row = r;
-        tk.head = h;
-        tk.fin = plan.fin;
-        tk.p0 = plan.p0;
-        for (int t = 0; t < plan.n; ++t) tk.alpha[t] = __ldg(rg + rec + t);
-        unsigned char* st = smem_raw + (size_t)s * stage_bytes;
-        const uint32_t nu = (uint32_t)(plan.n * V * 4), nk = (uint32_t)(plan.n * K * 4);
-        mbar_arrive_expect_tx(&full[s], state_bytes + nu + nk);
-        bulk_g2s(st, pool + ((size_t)plan.src * p.HV + h) * head, state_bytes, &full[s]);
-        bulk_g2s(st + state_bytes, ru + rec * V, nu, &full[s]);
-        bulk_g2s(st + state_bytes + u_bytes, rk + rec * K, nk, &full[s]);
-        ++it;
-      }
-    }
-    if (!ok) return;
-    // end-of-work ticket
-    const int s = (int)(it % (uint32_t)num_stages);
-    const uint32_t round = it / (uint32_t)num_stages;
-    if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1u)) {
-      if (p.err) atomicOr(p.err, kErrTimeout);
-      return;
-    }
-    tickets[s].n = -1;
-    mbar_arrive_expect_tx(&full[s], 0);
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int ct = threadIdx.x - 32;
-  const int col = (ct % CPR) * E;
-  const int nchunks = V * CPR;
-  for (uint32_t it = 0;; ++it) {
-    const int s = (int)(it % (uint32_t)num_stages);
-    const uint32_t round = it / (uint32_t)num_stages;
-    if (!mbar_wait(&full[s], round & 1u)) {
-      if (p.err && lane == 0) atomicOr(p.err, kErrTimeout);
-      return;
-    }
-    const StageTicket& tk = tickets[s];
-    const int n = tk.n;
-    if (n < 0) return;
-    const int layer = tk.layer, r = tk.row, h = tk.head, fin = tk.fin;
-    const long long p0 = tk.p0;
-    const unsigned char* st = smem_raw + (size_t)s * stage_bytes;
-    const ST* S = reinterpret_cast<const ST*>(st);
-    const float* u_s = reinterpret_cast<const float*>(st + state_bytes);
-    const float* k_s = reinterpret_cast<const float*>(st + state_bytes + u_bytes);
-
-    f32x2 x[M][E / 2];
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-      const int c = ct + NT * m;
-      if (c < nchunks) C::load_shared(S + (size_t)c * E, x[m]);
-    }
-    ST* pool = static_cast<ST*>(p.pools[layer]);
-    const int32_t* trow = p.slot_table + (size_t)r * p.table_stride;
-    for (int t = 0; t < n; ++t) {
-      fold_token<K, ST, M, NT>(x, tk.alpha[t], k_s, u_s, t, V, col, ct, 0, nchunks);
-      const long long pos = p0 + t + 1;
-      if (p.block_size > 0 && t + 1 < n && pos % p.block_size == 0) {
-        const int bs = slot_after(trow, p.table_stride, p.block_size, pos);
-        store_chunks<ST, M, NT>(pool + ((size_t)bs * p.HV + h) * head, x, ct, nchunks);
-      }
-    }
-    // every shared-memory read of this stage is done: hand it back
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    store_chunks<ST, M, NT>(pool + ((size_t)fin * p.HV + h) * head, x, ct, nchunks);
-  }
-}
-
 // --------------------------------------------------------------- launchers
-static int sm_count() {
-  static int num_sms[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev < 64 && num_sms[dev] == 0)
-    cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  return dev < 64 && num_sms[dev] > 0 ? num_sms[dev] : 148;
-}
-
-template <int K, typename ST>
-static int launch_commit_pipelined_k(const CommitParams& p, cudaStream_t stream) {
-  const size_t stage = (size_t)p.V * K * sizeof(ST) + (size_t)p.W * (p.V + K) * 4;
-  const size_t extra = kMaxStages * (sizeof(StageTicket) + 2 * sizeof(uint64_t));
-  const size_t budget = 227 * 1024 - extra;
-  int stages = (int)(budget / stage);
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2) return GDN_ERR_UNSUPPORTED;
-  const size_t smem = (size_t)stages * stage + extra;
-  if (cudaFuncSetAttribute(gdn_commit_pipelined_kernel<K, ST>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return GDN_ERR_CUDA;
-  const long long pairs = (long long)p.num_layers * p.batch;
-  const int sms = sm_count();
-  const int grid = (int)(pairs < sms ? pairs : sms);
-  gdn_commit_pipelined_kernel<K, ST><<<grid, kPipeThreads, smem, stream>>>(p, stages);
-  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-}
-
 template <int K, typename ST, int M>
 static int launch_commit_tiled_k(const CommitParams& p, cudaStream_t stream) {
   constexpr int CPR = K / Chunk<ST>::E;
@@ -431,23 +254,18 @@ static int launch_commit_tiled_k(const CommitParams& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// A tile is 64 state rows (8 chunks per thread for a 128-wide fp32 state,
+// 4 for bf16): four such CTAs fit on an SM, and measured against whole-head
+// and 32-row tiles, and against a persistent kernel streaming heads through
+// shared memory with bulk asynchronous copies, it moves the most bytes.
 template <int K, typename ST>
 static int launch_commit_k(const CommitParams& p, cudaStream_t stream) {
-  // M = chunks per thread; the default tile is 64 state rows (M = 8 for a
-  // 128-wide fp32 state, 4 for bf16).  GDN_COMMIT_VARIANT selects another
-  // schedule for measurement: 'p' pipelined, '4' / 'f' other tile sizes.
-  static const char* variant = getenv("GDN_COMMIT_VARIANT");
-  const char v = variant ? variant[0] : 'd';
   constexpr int CPR = K / Chunk<ST>::E;
   constexpr int MMAX = (128 * K) / Chunk<ST>::E / kCommitThreads;
   constexpr int MFULL = MMAX > 0 ? MMAX : 1;
   constexpr int M64 = (64 * CPR) / kCommitThreads;
-  constexpr int MDEF = M64 < 1 ? 1 : (M64 > MFULL ? MFULL : M64);
-  constexpr int M4 = MFULL < 4 ? MFULL : 4;
-  if (v == 'p') return launch_commit_pipelined_k<K, ST>(p, stream);
-  if (v == '4') return launch_commit_tiled_k<K, ST, M4>(p, stream);
-  if (v == 'f') return launch_commit_tiled_k<K, ST, MFULL>(p, stream);
-  return launch_commit_tiled_k<K, ST, MDEF>(p, stream);
+  constexpr int M = M64 < 1 ? 1 : (M64 > MFULL ? MFULL : M64);
+  return launch_commit_tiled_k<K, ST, M>(p, stream);
 }
 
 int launch_commit(const CommitParams& p, int head_k, int state_dtype, cudaStream_t stream) {

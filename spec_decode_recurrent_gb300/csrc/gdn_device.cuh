@@ -54,6 +54,9 @@ struct VerifyParams {
 struct CommitParams {
   int HV, V, W;
   int num_layers, batch, num_slots;
+  const int32_t* layer_group;  // [num_layers] or NULL (one group)
+  int num_groups;
+  long long group_stride;      // elements between two groups' slot tables
   void* const* pools;
   const float* const* rec_u;
   const float* const* rec_k;

@@ -324,3 +324,39 @@ def test_bf16_ulp_is_grid_spacing():
     assert np.array_equal(spacing, bf16_ulp(xb.double().numpy()))
     assert np.all(np.abs(xb.double().numpy() - x.double().numpy())
                   <= 0.5 * bf16_ulp(xb.double().numpy()) + 0.0)
+
+
+# ------------------------------------------------------- grouped commit
+def test_grouped_commit_reduces_to_per_layer_commits():
+    # Layers in KV-cache groups, each group with its own [batch, stride]
+    # slot table: the grouped commit must equal committing each layer on
+    # its own with its group's table.
+    g = np.random.default_rng(21)
+    L, G, B, HV, K, V, W, slots = 6, 3, 4, 2, 8, 8, 4, 12
+    pools = g.normal(0, 0.1, (L, slots, HV, V, K))
+    rec_u, rec_k = g.normal(size=(L, B, HV, W, V)), g.normal(size=(L, B, HV, W, K))
+    rec_g = g.uniform(0.1, 1.0, (L, B, HV, W))
+    win = np.array([4, 3, 0, 4], np.int32)
+    acc = np.array([2, 3, 0, 4], np.int32)
+    tables = np.stack([g.permutation(slots)[:B].reshape(B, 1) for _ in range(G)]).astype(np.int32)
+    tables[1, 3, 0] = -1                        # a null slot in one group only
+    layer_group = np.array([0, 1, 2, 0, 1, 2], np.int32)
+    got, err = oracle.replay_commit(pools=pools, rec_u=rec_u, rec_k=rec_k, rec_g=rec_g,
+                                    window_len=win, accepted_len=acc, slot_table=tables,
+                                    layer_group=layer_group, max_window=W)
+    assert np.all(err == 0)
+    for l in range(L):
+        one, e1 = oracle.replay_commit(pools=pools[l:l + 1], rec_u=rec_u[l:l + 1],
+                                       rec_k=rec_k[l:l + 1], rec_g=rec_g[l:l + 1],
+                                       window_len=win, accepted_len=acc,
+                                       slot_table=tables[layer_group[l]], max_window=W)
+        assert np.array_equal(got[l], one[0])
+    # one group whose table every layer shares is the plain all-layer commit
+    plain, _ = oracle.replay_commit(pools=pools, rec_u=rec_u, rec_k=rec_k, rec_g=rec_g,
+                                    window_len=win, accepted_len=acc, slot_table=tables[0],
+                                    max_window=W)
+    same, _ = oracle.replay_commit(pools=pools, rec_u=rec_u, rec_k=rec_k, rec_g=rec_g,
+                                   window_len=win, accepted_len=acc,
+                                   slot_table=np.stack([tables[0]] * G),
+                                   layer_group=layer_group, max_window=W)
+    assert np.array_equal(plain, same)
