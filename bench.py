@@ -62,6 +62,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layers", type=int, default=None,
                    help="fewer layers (for small profiler captures; not a bench line)")
+    p.add_argument("--grouped-commit", action="store_true",
+                   help="measure the grouped commit (3 KV-cache groups x 6 layers, one launch) "
+                        "against one commit call per group; prints its own JSON line")
     return p.parse_args()
 
 
@@ -253,6 +256,8 @@ def run_gpu(args, rank, local_rank, world_size):
     nbytes = roofline.native_bytes_per_layer(sb)
     del out_n, snaps
 
+    conv = run_conv_commit(sb, stream, peak)
+
     e2e = None if args.no_e2e else run_e2e(args, sb, bufs, graph, stream, arena)
 
     result = {
@@ -290,6 +295,7 @@ def run_gpu(args, rank, local_rank, world_size):
             "achieved_gbs": round(nbytes / (native_us * 1e-6) / 1e9, 1),
             "note": "comparison baseline, not part of the step",
         },
+        "conv_commit": conv,
         "gpu_launches": K * (sb.L + 1),
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
@@ -299,6 +305,42 @@ def run_gpu(args, rank, local_rank, world_size):
     if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(sb, args.cpu_seconds)
     return result
+
+
+def run_conv_commit(sb, stream, peak, state_len=3):
+    """Short-conv state commit of every layer (bf16 states, width-4
+    convolution) with the step's plan: one launch, timed from a CUDA graph
+    replayed back to back.  Reported beside the step, not inside it."""
+    pools, inputs = workloads.conv_state(sb, state_len=state_len, dtype=torch.bfloat16)
+    tab = api.ConvTable(pools, inputs)
+
+    def call():
+        api.gdn_conv_state_commit(table=tab, token_start=sb.token_start, window_len=sb.window_len,
+                                  accepted_len=sb.accepted_len, slot_tables=sb.slot_table,
+                                  max_window=sb.W, seq_pos=sb.seq_pos, block_size=sb.block_size)
+
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for _ in range(3):
+        g.replay()
+    reps = 50
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / reps
+    C = tab.C
+    nbytes = roofline.conv_commit_bytes(sb, C, state_len, 2)
+    del pools, inputs, tab, g
+    return {"kernel": "gdn_conv_commit_kernel", "us": round(us, 2), "channels": C,
+            "state_len": state_len, "dtype": "bf16", "algorithmic_bytes": nbytes,
+            "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)}
 
 
 def run_e2e(args, sb, bufs, graph, stream, arena):
@@ -335,6 +377,76 @@ def run_e2e(args, sb, bufs, graph, stream, arena):
             "d2h_bytes_per_step": bo, "steps": E,
             "path": "one pinned host -> device copy of every input of the step, verify graph + "
                     "commit call, one device -> host copy of every layer's output, error word"}
+
+
+def run_grouped(args):
+    """Grouped all-layer commit: 18 GDN layers in 3 KV-cache groups of 6, each
+    group with its own state-index table, committed by one grouped launch or
+    by one commit call per group.  Device time by CUDA events, host time of
+    the calls by the wall clock (the calls enqueue and return)."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build.build()
+    api.load()
+    G, per = 3, 6
+    sb = workloads.all_layer(device=dev, sentinel=False, L=G * per)
+    gen = torch.Generator().manual_seed(11)
+    tables = [sb.slot_table.cpu()]
+    for _ in range(1, G):
+        perm = torch.randperm(sb.num_slots, generator=gen)[:sb.B].view(-1, 1).to(torch.int32)
+        perm[sb.window_len.cpu() == 0] = -1
+        tables.append(perm)
+    slot_tables = torch.stack(tables).to(dev).contiguous()
+    layer_group = torch.tensor([l // per for l in range(sb.L)], dtype=torch.int32, device=dev)
+    bufs = step.StepBuffers(sb)
+    for l in range(sb.L):
+        g = l // per
+        api.gdn_spec_verify(q=sb.q[l], k=sb.k[l], v=sb.v[l], a=sb.a[l], b=sb.b[l],
+                            A_log=sb.A_log[l], dt_bias=sb.dt_bias[l], token_start=sb.token_start,
+                            window_len=sb.window_len, state_pool=sb.pools[l],
+                            slot_table=slot_tables[g], out=bufs.out[l], rec_u=bufs.rec_u[l],
+                            rec_k=bufs.rec_k[l], rec_g=bufs.rec_g[l], max_window=sb.W,
+                            err=bufs.err)
+    group_tabs = [api.LayerTable(sb.pools[g * per:(g + 1) * per], bufs.rec_u[g * per:(g + 1) * per],
+                                 bufs.rec_k[g * per:(g + 1) * per], bufs.rec_g[g * per:(g + 1) * per])
+                  for g in range(G)]
+
+    def grouped():
+        api.gdn_replay_commit_grouped(table=bufs.table, num_k_heads=sb.HK, layer_group=layer_group,
+                                      window_len=sb.window_len, accepted_len=sb.accepted_len,
+                                      slot_tables=slot_tables, err=bufs.err)
+
+    def per_group():
+        for g in range(G):
+            api.gdn_replay_commit(table=group_tabs[g], num_k_heads=sb.HK, window_len=sb.window_len,
+                                  accepted_len=sb.accepted_len, slot_table=slot_tables[g],
+                                  err=bufs.err)
+
+    stream = torch.cuda.current_stream()
+    out = {"impl": "gb300", "measurement": "grouped all-layer commit",
+           "config": {"workload": f"{G} KV-cache groups x {per} GDN layers, all_layer shapes "
+                                  "(batch 64 with 8 padding rows, HK=16 HV=32 K=V=128, window 4)"}}
+    cbytes = roofline.commit_bytes(sb)
+    for name, fn in (("grouped_one_launch", grouped), ("one_call_per_group", per_group)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        K = max(20, args.steps // 10)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        host = 0.0
+        a.record(stream)
+        for _ in range(K):
+            t0 = time.perf_counter()
+            fn()
+            host += time.perf_counter() - t0
+        b.record(stream)
+        torch.cuda.synchronize()
+        dev_us = a.elapsed_time(b) * 1e3 / K
+        out[name] = {"device_us": round(dev_us, 2), "host_us_per_step": round(host / K * 1e6, 2),
+                     "launches_per_step": 1 if name.startswith("grouped") else G,
+                     "achieved_gbs": round(cbytes / (dev_us * 1e-6) / 1e9, 1)}
+    assert int(bufs.err.item()) == 0
+    return out
 
 
 # ---------------------------------------------------- CPU oracle timing
@@ -455,6 +567,9 @@ def main():
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args, rank, world_size)), flush=True)
+        return 0
+    if args.grouped_commit:
+        print(json.dumps(run_grouped(args)), flush=True)
         return 0
     rank, local_rank, world_size = dist.init("nccl")
     try:

@@ -196,6 +196,45 @@ int gdn_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers,
                               int32_t* err, void* stream);
 
 /*
+ * Short-conv state commit over all layers in one launch (vLLM PR above,
+ * Purpose: the short conv compacts its accepted window with the same plan;
+ * Commits item 1: the commit's plan, conv and state steps).  A layer's
+ * causal depthwise convolution of width state_len + 1 keeps, per slot and
+ * channel, the last state_len convolution inputs, oldest first.  For each
+ * live row with n = accepted_len[r] > 0 the state after x tokens -- the last
+ * state_len entries of (checkpoint state ++ the row's first x inputs) -- is
+ * written to the slots gdn_replay_commit writes for x = n (and, in align
+ * mode, for each boundary).  Pure copies: results are bit-exact.
+ *
+ *   channels, state_len  C >= 1, 1 <= state_len <= 8; dtype: element type of
+ *                  both the state and the inputs (F32 or BF16).
+ *   conv_pools     device array [num_layers] of device pointers to
+ *                  [num_slots][C][state_len] states, updated in place.
+ *   conv_inputs    device array [num_layers] of device pointers to the
+ *                  layer's convolution inputs, one row of C elements per
+ *                  token row, rows input_row_stride elements apart.
+ *   token_start    [batch]: first token row of each request's window.
+ *   layer_group / num_groups / slot_tables / group_stride as in
+ *                  gdn_replay_commit_grouped (num_groups = 1 and layer_group
+ *                  NULL for a single table).
+ * Row errors as for the commit, plus GDN_ROW_ERR_TOKENS for window rows
+ * outside [0, num_tokens).
+ */
+int gdn_conv_state_commit(int32_t num_layers, int32_t num_groups,
+                          const int32_t* layer_group, int32_t batch,
+                          int32_t num_tokens, int32_t num_slots,
+                          int32_t channels, int32_t state_len, int32_t dtype,
+                          int32_t max_window, void* const* conv_pools,
+                          const void* const* conv_inputs,
+                          int64_t input_row_stride, const int32_t* token_start,
+                          const int32_t* window_len,
+                          const int32_t* accepted_len,
+                          const int32_t* slot_tables,
+                          int32_t slot_table_stride, int64_t group_stride,
+                          const int32_t* seq_pos, int32_t block_size,
+                          int32_t* err, void* stream);
+
+/*
  * Native baseline of one layer: the verify's recurrence with the full
  * state stored after every draft position, and no record (vLLM PR above,
  * Purpose: the path that snapshots the recurrent state after every draft

@@ -80,6 +80,9 @@ def _load():
             lib.gdn_oracle_replay_commit_grouped.restype = _i
             lib.gdn_oracle_replay_commit_grouped.argtypes = (
                 [_i] * 7 + [_D] * 5 + [_I, _I, _I, _i, ctypes.c_long, _I, _i, _I, _i, _I])
+            lib.gdn_oracle_conv_commit.restype = _i
+            lib.gdn_oracle_conv_commit.argtypes = (
+                [_i] * 7 + [_D] * 3 + [_I, _I, _I, _I, _i, ctypes.c_long, _I, _i, _I, _i, _I])
             lib.gdn_oracle_num_threads.restype = _i
             lib.gdn_oracle_num_threads.argtypes = []
             _lib = lib
@@ -268,4 +271,38 @@ def replay_commit(*, pools, rec_u, rec_k, rec_g, window_len, accepted_len, slot_
         slot_table.shape[2], _ip(sp), int(block_size), _ip(row_err))
     if rc != 0:
         raise ValueError(f"oracle replay_commit rejected the shape ({rc})")
+    return pools_out, row_err
+
+
+def conv_commit(*, pools, inputs, token_start, window_len, accepted_len, slot_table,
+                seq_pos=None, block_size=0, max_window, layer_group=None):
+    """Short-conv state commit.
+
+    pools [L, num_slots, C, SL] (last SL conv inputs per channel, oldest
+    first); inputs [L, T, C]; slot_table [B, stride] or [G, B, stride] with
+    layer_group [L].  Returns (new_pools float64, row_err).
+    """
+    pools_in = _f64(pools)
+    pools_out = pools_in.copy()
+    inputs = _f64(inputs)
+    token_start, window_len, accepted_len = _i32(token_start), _i32(window_len), _i32(accepted_len)
+    slot_table = _i32(slot_table)
+    if slot_table.ndim == 1:
+        slot_table = slot_table.reshape(-1, 1)
+    if slot_table.ndim == 2:
+        slot_table = slot_table[None]
+    G = slot_table.shape[0]
+    lg = None if layer_group is None else _i32(layer_group)
+    L, num_slots, C, SL = pools_in.shape
+    T = inputs.shape[1]
+    B = window_len.shape[0]
+    sp = None if seq_pos is None else _i32(seq_pos)
+    row_err = np.zeros(B, dtype=np.int32)
+    rc = _load().gdn_oracle_conv_commit(
+        L, C, SL, int(max_window), B, T, num_slots, _dp(pools_in), _dp(pools_out), _dp(inputs),
+        _ip(token_start), _ip(window_len), _ip(accepted_len), _ip(lg), G,
+        slot_table.shape[1] * slot_table.shape[2], _ip(slot_table), slot_table.shape[2], _ip(sp),
+        int(block_size), _ip(row_err))
+    if rc != 0:
+        raise ValueError(f"oracle conv_commit rejected the shape ({rc})")
     return pools_out, row_err

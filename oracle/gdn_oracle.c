@@ -400,3 +400,62 @@ int gdn_oracle_replay_commit(int L, int HV, int K, int V, int W_max, int B,
       rec_g, window_len, accepted_len, NULL, 1, 0, slot_table, table_stride,
       seq_pos, block_size, row_err);
 }
+
+/* Short-conv state commit (vLLM PR above, Purpose: the short conv "compacts
+ * its accepted window with the same plan").  A layer's causal depthwise
+ * convolution of width SL + 1 keeps, per slot and channel, the last SL
+ * convolution inputs, oldest first: state [C][SL].  The state after x
+ * folded tokens of a row is the last SL entries of
+ *     (checkpoint state of the channel) ++ (the row's first x window inputs),
+ * written to the slots the SSM commit plan names for x tokens.
+ *   pools_in / pools_out [L][num_slots][C][SL]   (pools_out: caller's copy)
+ *   inputs [L][T][C]: convolution inputs of every token row
+ *   token_start[B]: first token row of each request's window
+ * Row errors are the commit plan's, then GDN_ROW_ERR_TOKENS when a live
+ * row's window rows fall outside [0, T). */
+int gdn_oracle_conv_commit(int L, int C, int SL, int W_max, int B, int T,
+                           int num_slots, const double* pools_in,
+                           double* pools_out, const double* inputs,
+                           const int32_t* token_start,
+                           const int32_t* window_len,
+                           const int32_t* accepted_len,
+                           const int32_t* layer_group, int num_groups,
+                           long group_stride, const int32_t* slot_table,
+                           int table_stride, const int32_t* seq_pos,
+                           int block_size, int32_t* row_err) {
+  if (L <= 0 || C <= 0 || SL <= 0 || W_max <= 0 || num_groups <= 0) return -2;
+  if (layer_group)
+    for (int l = 0; l < L; ++l)
+      if (layer_group[l] < 0 || layer_group[l] >= num_groups) return -3;
+  size_t pool_elems = (size_t)num_slots * C * SL;
+  int max_writes = 2 + W_max;
+  for (int r = 0; r < B; ++r) row_err[r] = 0;
+  double* seq = (double*)malloc((size_t)(SL + W_max) * sizeof(double));
+  for (int l = 0; l < L; ++l) {
+    int g = layer_group ? layer_group[l] : 0;
+    for (int r = 0; r < B; ++r) {
+      int32_t src, slots[64], ntok[64];
+      int sp = seq_pos ? seq_pos[r] : 0;
+      const int32_t* trow = slot_table + g * group_stride + (size_t)r * table_stride;
+      int nw = gdn_oracle_commit_plan(window_len[r], accepted_len[r], trow,
+                                      table_stride, sp, block_size, num_slots,
+                                      W_max, &src, slots, ntok, max_writes);
+      if (nw < 0) { row_err[r] |= -nw - 1; continue; }
+      if (nw == 0) continue;
+      long t0 = token_start[r];
+      if (t0 < 0 || t0 + window_len[r] > T) { row_err[r] |= ORACLE_ERR_TOKENS; continue; }
+      for (int c = 0; c < C; ++c) {
+        const double* old = pools_in + l * pool_elems + ((size_t)src * C + c) * SL;
+        for (int j = 0; j < SL; ++j) seq[j] = old[j];
+        for (int i = 0; i < accepted_len[r]; ++i)
+          seq[SL + i] = inputs[((size_t)l * T + t0 + i) * C + c];
+        for (int w = 0; w < nw; ++w) {
+          double* dst = pools_out + l * pool_elems + ((size_t)slots[w] * C + c) * SL;
+          for (int j = 0; j < SL; ++j) dst[j] = seq[ntok[w] + j];
+        }
+      }
+    }
+  }
+  free(seq);
+  return 0;
+}

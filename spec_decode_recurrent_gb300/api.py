@@ -22,7 +22,7 @@ ROW_ERR_WINDOW, ROW_ERR_ACCEPTED, ROW_ERR_SLOT = 1, 2, 4
 ROW_ERR_BLOCK, ROW_ERR_SEQPOS, ROW_ERR_TOKENS = 8, 16, 32
 ROW_ERR_GROUP = 64
 ENTRY_POINTS = ("gdn_spec_verify", "gdn_replay_commit", "gdn_replay_commit_grouped",
-                "gdn_native_spec_snapshot")
+                "gdn_conv_state_commit", "gdn_native_spec_snapshot")
 
 _ERRORS = {-1: "null pointer", -2: "unsupported shape or dtype",
            -3: "invalid count, stride, alignment or block size", -4: "CUDA launch failed"}
@@ -70,6 +70,10 @@ def load() -> ctypes.CDLL:
             lib.gdn_replay_commit.argtypes = [ctypes.POINTER(gdn_shape), _I32, _I32, _I32,
                                               _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32,
                                               _P, _P]
+            lib.gdn_conv_state_commit.restype = ctypes.c_int
+            lib.gdn_conv_state_commit.argtypes = [
+                _I32, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I64, _P, _P,
+                _P, _P, _I32, _I64, _P, _I32, _P, _P]
             lib.gdn_replay_commit_grouped.restype = ctypes.c_int
             lib.gdn_replay_commit_grouped.argtypes = [
                 ctypes.POINTER(gdn_shape), _I32, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
@@ -267,3 +271,60 @@ def gdn_replay_commit_grouped(*, table: LayerTable, num_k_heads: int, layer_grou
         _ptr(seq_pos if block_size else None), int(block_size), _ptr(err), _stream(stream))
     if rc != 0:
         raise GDNError("gdn_replay_commit_grouped", rc)
+
+
+class ConvTable:
+    """Device arrays of per-layer pointers for the short-conv state commit:
+    pools [num_slots, C, SL] and the layer's convolution inputs [T, C]
+    (token rows may be strided; every layer the same row stride)."""
+
+    def __init__(self, pools: Sequence[torch.Tensor], inputs: Sequence[torch.Tensor]):
+        _need(len(pools) >= 1 and len(pools) == len(inputs), "one pool and one input per layer")
+        p0, x0 = pools[0], inputs[0]
+        for t in pools:
+            _contig(t, "conv pool", p0.dtype)
+            _need(t.shape == p0.shape and t.dim() == 3, "conv pools must share [slots, C, SL]")
+        for x in inputs:
+            _need(x.is_cuda and x.dim() == 2 and x.dtype == p0.dtype and x.stride(1) == 1,
+                  "conv inputs must be [T, C] rows of the pools' dtype")
+            _need(x.shape == x0.shape and x.stride(0) == x0.stride(0), "conv inputs must share layout")
+        _need(x0.shape[1] == p0.shape[1], "conv inputs must have C channels")
+        dev = p0.device
+        mk = lambda ts: torch.tensor([t.data_ptr() for t in ts], dtype=torch.int64, device=dev)
+        self.pools, self.inputs = list(pools), list(inputs)
+        self.d_pools, self.d_inputs = mk(pools), mk(inputs)
+        self.num_layers = len(pools)
+        self.num_slots, self.C, self.SL = p0.shape
+        self.dtype = p0.dtype
+        self.num_tokens = x0.shape[0]
+        self.in_stride = x0.stride(0) if x0.shape[0] > 1 else x0.shape[1]
+
+
+def gdn_conv_state_commit(*, table: ConvTable, token_start, window_len, accepted_len,
+                          slot_tables, max_window, layer_group=None, seq_pos=None,
+                          block_size=0, err=None, stream=None) -> None:
+    """Short-conv state commit of every layer in one launch, with the same
+    plan as the recurrent-state commit."""
+    B = window_len.shape[0]
+    for name, t in (("token_start", token_start), ("window_len", window_len),
+                    ("accepted_len", accepted_len)):
+        _contig(t, name, torch.int32)
+        _need(t.shape == (B,), f"{name} must be [batch]")
+    st = slot_tables if slot_tables.dim() == 3 else slot_tables.view(1, B, -1)
+    _contig(st, "slot_tables", torch.int32)
+    G, _, stride = st.shape
+    if layer_group is not None:
+        _contig(layer_group, "layer_group", torch.int32)
+        _need(layer_group.shape == (table.num_layers,), "layer_group must be [num_layers]")
+    if block_size:
+        _contig(seq_pos, "seq_pos", torch.int32)
+    if err is not None:
+        _contig(err, "err", torch.int32)
+    rc = load().gdn_conv_state_commit(
+        table.num_layers, G, _ptr(layer_group), B, table.num_tokens, table.num_slots, table.C,
+        table.SL, _dtype_code(table.dtype), int(max_window), _ptr(table.d_pools),
+        _ptr(table.d_inputs), table.in_stride, _ptr(token_start), _ptr(window_len),
+        _ptr(accepted_len), _ptr(st), stride, B * stride, _ptr(seq_pos if block_size else None),
+        int(block_size), _ptr(err), _stream(stream))
+    if rc != 0:
+        raise GDNError("gdn_conv_state_commit", rc)

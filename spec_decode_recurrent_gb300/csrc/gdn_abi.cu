@@ -205,4 +205,51 @@ int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
                                    slot_table_stride, 0, seq_pos, block_size, err, stream);
 }
 
+int gdn_conv_state_commit(int32_t num_layers, int32_t num_groups, const int32_t* layer_group,
+                          int32_t batch, int32_t num_tokens, int32_t num_slots, int32_t channels,
+                          int32_t state_len, int32_t dtype, int32_t max_window,
+                          void* const* conv_pools, const void* const* conv_inputs,
+                          int64_t input_row_stride, const int32_t* token_start,
+                          const int32_t* window_len, const int32_t* accepted_len,
+                          const int32_t* slot_tables, int32_t slot_table_stride,
+                          int64_t group_stride, const int32_t* seq_pos, int32_t block_size,
+                          int32_t* err, void* stream) {
+  if (channels < 1 || state_len < 1 || state_len > 8 || !valid_dtype(dtype) || max_window < 1 ||
+      max_window > gdn::kMaxWindow)
+    return GDN_ERR_UNSUPPORTED;
+  if (batch == 0) return GDN_OK;
+  if (!conv_pools || !conv_inputs || !token_start || !window_len || !accepted_len || !slot_tables)
+    return GDN_ERR_NULL;
+  if (num_groups > 1 && !layer_group) return GDN_ERR_NULL;
+  if (block_size > 0 && !seq_pos) return GDN_ERR_NULL;
+  if (num_layers < 1 || num_layers > 65535 || batch < 0 || batch > 65535 || num_slots < 0 ||
+      num_tokens < 0 || num_groups < 1 || block_size < 0 || slot_table_stride < 1 ||
+      input_row_stride < channels)
+    return GDN_ERR_INVALID;
+  if (num_groups > 1 && group_stride < (int64_t)batch * slot_table_stride) return GDN_ERR_INVALID;
+  gdn::ConvParams p;
+  p.num_layers = num_layers;
+  p.batch = batch;
+  p.num_slots = num_slots;
+  p.num_tokens = num_tokens;
+  p.C = channels;
+  p.SL = state_len;
+  p.W = max_window;
+  p.layer_group = layer_group;
+  p.num_groups = num_groups;
+  p.group_stride = num_groups > 1 ? group_stride : 0;
+  p.pools = conv_pools;
+  p.inputs = conv_inputs;
+  p.in_stride = input_row_stride;
+  p.token_start = token_start;
+  p.window_len = window_len;
+  p.accepted_len = accepted_len;
+  p.slot_table = slot_tables;
+  p.table_stride = slot_table_stride;
+  p.seq_pos = seq_pos;
+  p.block_size = block_size;
+  p.err = err;
+  return gdn::launch_conv_commit(p, dtype, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

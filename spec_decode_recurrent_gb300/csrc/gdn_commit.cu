@@ -30,17 +30,6 @@
 
 namespace gdn {
 
-// Commit plan of one request row: checkpoint slot, final slot, accepted
-// length and row errors, in the documented order of checks.  Boundary
-// slots are validated here and looked up again when they are written.
-struct RowCommit {
-  int err;       // GDN_ROW_ERR_* bits
-  bool live;     // something to fold and store
-  int src, fin;  // checkpoint slot, final slot
-  int n;         // accepted tokens
-  long long p0;  // tokens already in the checkpoint (align mode)
-};
-
 // Slot-table row of request r for the group of `layer`, or NULL when the
 // layer's group id is outside [0, num_groups).
 __device__ __forceinline__ const int32_t* group_table_row(const CommitParams& p, int layer,
@@ -52,33 +41,8 @@ __device__ __forceinline__ const int32_t* group_table_row(const CommitParams& p,
 
 __device__ __forceinline__ RowCommit commit_row_plan(const CommitParams& p, int r,
                                                      const int32_t* trow) {
-  RowCommit c{0, false, -1, -1, 0, 0};
-  if (trow == nullptr) { c.err = GDN_ROW_ERR_GROUP; return c; }
-  const int w = p.window_len[r];
-  const int n = p.accepted_len[r];
-  SourceSlot src = source_slot(w, p.W, trow, p.table_stride, p.block_size, p.seq_pos, r,
-                               p.num_slots);
-  if (src.err) { c.err = src.err; return c; }
-  if (n < 0 || n > w) { c.err = GDN_ROW_ERR_ACCEPTED; return c; }
-  if (src.slot < 0 || n == 0) return c;
-  const long long p0 = p.block_size > 0 ? p.seq_pos[r] : 0;
-  const int fin = slot_after(trow, p.table_stride, p.block_size, p0 + n);
-  if (fin == kOutsideTable || fin == -1) { c.err = GDN_ROW_ERR_BLOCK; return c; }
-  if (fin < -1 || fin >= p.num_slots) { c.err = GDN_ROW_ERR_SLOT; return c; }
-  if (p.block_size > 0) {
-    for (int j = 1; j < n; ++j) {
-      if ((p0 + j) % p.block_size != 0) continue;
-      const int bs = slot_after(trow, p.table_stride, p.block_size, p0 + j);
-      if (bs == kOutsideTable || bs == -1) { c.err = GDN_ROW_ERR_BLOCK; return c; }
-      if (bs < -1 || bs >= p.num_slots) { c.err = GDN_ROW_ERR_SLOT; return c; }
-    }
-  }
-  c.live = true;
-  c.src = src.slot;
-  c.fin = fin;
-  c.n = n;
-  c.p0 = p0;
-  return c;
+  return row_commit_plan(p.window_len[r], p.accepted_len[r], trow, p.table_stride,
+                         p.block_size, p.seq_pos, r, p.num_slots, p.W);
 }
 
 // A 16-byte chunk of state (4 fp32 or 8 bf16) as packed fp32 pairs.

@@ -70,6 +70,25 @@ struct CommitParams {
   int32_t* err;
 };
 
+struct ConvParams {
+  int num_layers, batch, num_slots, num_tokens;
+  int C, SL, W;                  // channels, state length, max window
+  const int32_t* layer_group;    // [num_layers] or NULL (one group)
+  int num_groups;
+  long long group_stride;
+  void* const* pools;            // [num_layers] -> [num_slots][C][SL]
+  const void* const* inputs;     // [num_layers] -> token rows of C inputs
+  long long in_stride;           // elements between token rows
+  const int32_t* token_start;
+  const int32_t* window_len;
+  const int32_t* accepted_len;
+  const int32_t* slot_table;
+  int table_stride;
+  const int32_t* seq_pos;
+  int block_size;
+  int32_t* err;
+};
+
 // ----------------------------------------------------------------- gates
 // softplus(x) = log(1 + e^x), in the form that does not overflow.
 __device__ __forceinline__ float softplus(float x) {
@@ -241,6 +260,48 @@ __device__ __forceinline__ SourceSlot source_slot(int w, int W, const int32_t* r
   if (slot < -1 || slot >= num_slots) { s.err = GDN_ROW_ERR_SLOT; return s; }
   s.slot = slot;
   return s;
+}
+
+// Commit plan of one request row: checkpoint slot, final slot, accepted
+// length and row errors, in the documented order of checks.  trow is the
+// row of the layer's slot table, NULL for a layer with a bad group id.
+// Boundary slots are validated here and looked up again when written.
+struct RowCommit {
+  int err;       // GDN_ROW_ERR_* bits
+  bool live;     // something to fold and store
+  int src, fin;  // checkpoint slot, final slot
+  int n;         // accepted tokens
+  long long p0;  // tokens already in the checkpoint (align mode)
+};
+
+__device__ __forceinline__ RowCommit row_commit_plan(int w, int n, const int32_t* trow,
+                                                     int stride, int block_size,
+                                                     const int32_t* seq_pos, int r,
+                                                     int num_slots, int W) {
+  RowCommit c{0, false, -1, -1, 0, 0};
+  if (trow == nullptr) { c.err = GDN_ROW_ERR_GROUP; return c; }
+  SourceSlot src = source_slot(w, W, trow, stride, block_size, seq_pos, r, num_slots);
+  if (src.err) { c.err = src.err; return c; }
+  if (n < 0 || n > w) { c.err = GDN_ROW_ERR_ACCEPTED; return c; }
+  if (src.slot < 0 || n == 0) return c;
+  const long long p0 = block_size > 0 ? seq_pos[r] : 0;
+  const int fin = slot_after(trow, stride, block_size, p0 + n);
+  if (fin == kOutsideTable || fin == -1) { c.err = GDN_ROW_ERR_BLOCK; return c; }
+  if (fin < -1 || fin >= num_slots) { c.err = GDN_ROW_ERR_SLOT; return c; }
+  if (block_size > 0) {
+    for (int j = 1; j < n; ++j) {
+      if ((p0 + j) % block_size != 0) continue;
+      const int bs = slot_after(trow, stride, block_size, p0 + j);
+      if (bs == kOutsideTable || bs == -1) { c.err = GDN_ROW_ERR_BLOCK; return c; }
+      if (bs < -1 || bs >= num_slots) { c.err = GDN_ROW_ERR_SLOT; return c; }
+    }
+  }
+  c.live = true;
+  c.src = src.slot;
+  c.fin = fin;
+  c.n = n;
+  c.p0 = p0;
+  return c;
 }
 
 }  // namespace gdn

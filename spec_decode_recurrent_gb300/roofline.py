@@ -75,3 +75,18 @@ def verify_flops_per_layer(sb: SpecBatch) -> int:
     """fp32 operations of the recurrence (decay multiply, two dot products,
     rank-1 update: 4 per state element per token, an FMA counted once)."""
     return sum(sb.HV * w * 4 * sb.V * sb.K for r, w, n, p0 in _rows(sb))
+
+
+def conv_commit_bytes(sb: SpecBatch, C: int, state_len: int, elem_bytes: int) -> int:
+    """Short-conv state commit: per live (layer, row) C*SL*e read, n*C*e
+    inputs read and (1 + boundaries)*C*SL*e written."""
+    S = C * state_len * elem_bytes
+    total = 0
+    for r, w, n, p0 in _rows(sb):
+        if n <= 0:
+            continue
+        bounds = 0
+        if sb.block_size > 0:
+            bounds = sum(1 for j in range(1, n) if (p0 + j) % sb.block_size == 0)
+        total += S + n * C * elem_bytes + (1 + bounds) * S
+    return total * sb.L

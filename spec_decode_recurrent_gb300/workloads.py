@@ -319,3 +319,22 @@ def custom(device="cpu", sentinel=True, seed=100, *, HK, HV, K, V, W, L, windows
                  seq_pos=seq_pos, block_size=block_size, qkv_dtype=qkv_dtype,
                  state_dtype=state_dtype, gen=gen, device=device, sentinel=sentinel,
                  gate_range=gate_range, gaps=gaps, row_order=order, fused=fused)
+
+
+def conv_state(sb: SpecBatch, state_len: int = 3, dtype=BF16, seed: int = 200):
+    """Short-conv states and inputs for every layer of a step: per layer a
+    pool [num_slots, C, state_len] ~ N(0, 1) and the convolution inputs of
+    every token row, C = 2*HK*K + HV*V channels.  The inputs are the fused
+    projection rows when the step has them, else fresh N(0, 1) rows."""
+    C = 2 * sb.HK * sb.K + sb.HV * sb.V
+    gen = _gen(seed, sb.device)
+    pools, inputs = [], []
+    for l in range(sb.L):
+        pools.append(torch.randn((sb.num_slots, C, state_len), generator=gen, device=sb.device,
+                                 dtype=F32).to(dtype))
+        if sb.fused_qkv is not None and sb.fused_qkv[l].dtype == dtype:
+            inputs.append(sb.fused_qkv[l])
+        else:
+            inputs.append(torch.randn((sb.T, C), generator=gen, device=sb.device,
+                                      dtype=F32).to(dtype))
+    return pools, inputs

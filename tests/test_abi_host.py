@@ -109,3 +109,24 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(api, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         api.load()
+
+
+def test_conv_commit_rejects_before_launch(lib):
+    def conv(**over):
+        a = dict(L=2, G=1, lg=None, B=4, T=16, slots=8, C=64, SL=3, dt=1, W=4, pools=FAKE,
+                 inputs=FAKE, ins=64, ts=FAKE, wl=FAKE, al=FAKE, st=FAKE, sts=1, gs=4, sp=None,
+                 bs=0)
+        a.update(over)
+        return lib.gdn_conv_state_commit(*[a[k] for k in (
+            "L", "G", "lg", "B", "T", "slots", "C", "SL", "dt", "W", "pools", "inputs", "ins",
+            "ts", "wl", "al", "st", "sts", "gs", "sp", "bs")], None, None)
+    assert conv(SL=9) == -2
+    assert conv(SL=0) == -2
+    assert conv(dt=5) == -2
+    assert conv(W=17) == -2
+    assert conv(pools=None) == -1
+    assert conv(ts=None) == -1
+    assert conv(G=2) == -1                      # groups need layer_group
+    assert conv(bs=4) == -1                     # align mode needs seq_pos
+    assert conv(ins=32) == -3                   # row stride shorter than C
+    assert conv(L=0) == -3

@@ -30,6 +30,8 @@ MUTANTS = {
     "replay_decays_after_write": (
         "double h = S[(size_t)i * K + j] * alpha[t];\n        S[(size_t)i * K + j] = h + ut[i] * kt[j];",
         "double h = S[(size_t)i * K + j];\n        S[(size_t)i * K + j] = (h + ut[i] * kt[j]) * alpha[t];"),
+    "conv_window_off_by_one": ("for (int j = 0; j < SL; ++j) dst[j] = seq[ntok[w] + j];",
+                               "for (int j = 0; j < SL; ++j) dst[j] = seq[ntok[w] + j - (j > 0)];"),
     "layer_group_ignored": ("int g = layer_group ? layer_group[l] : 0;", "int g = 0;"),
     "source_one_token_late": (
         "int32_t s = slot_after(table_row, table_stride, block_size, seq_pos);",

@@ -360,3 +360,66 @@ def test_grouped_commit_reduces_to_per_layer_commits():
                                    slot_table=np.stack([tables[0]] * G),
                                    layer_group=layer_group, max_window=W)
     assert np.array_equal(plain, same)
+
+
+# ------------------------------------------------------ short-conv commit
+def _shift_register(old, xs):
+    """Brute force: push the accepted inputs one at a time into a shift
+    register that drops its oldest entry."""
+    state = list(old)
+    for x in xs:
+        state = state[1:] + [x]
+    return state
+
+
+@pytest.mark.parametrize("SL", [1, 3, 5])
+def test_conv_commit_matches_shift_register(SL):
+    g = np.random.default_rng(SL)
+    C, W, B, slots = 6, 6, 5, 9
+    win = np.array([6, 4, 0, 1, 6], np.int32)
+    acc = np.array([6, 2, 0, 1, 0], np.int32)
+    starts = np.array([0, 7, 11, 11, 13], np.int32)       # rows with gaps, any order
+    T = 20
+    pools = g.normal(size=(1, slots, C, SL))
+    inputs = g.normal(size=(1, T, C))
+    table = np.array([[3], [0], [-1], [5], [7]], np.int32)
+    got, err = oracle.conv_commit(pools=pools, inputs=inputs, token_start=starts, window_len=win,
+                                  accepted_len=acc, slot_table=table, max_window=W)
+    assert np.all(err == 0)
+    expect = pools.copy()
+    for r in range(B):
+        s = table[r, 0]
+        if s < 0 or acc[r] == 0:
+            continue
+        for c in range(C):
+            xs = [inputs[0, starts[r] + i, c] for i in range(acc[r])]
+            expect[0, s, c] = _shift_register(list(pools[0, s, c]), xs)
+    assert np.array_equal(got, expect)
+
+
+def test_conv_commit_composes_and_aligns():
+    # committing n1 tokens and then n2 more from the new checkpoint equals
+    # committing n1 + n2 at once; align mode writes each block's last state
+    g = np.random.default_rng(3)
+    C, SL, W, slots = 4, 3, 6, 8
+    pools = g.normal(size=(1, slots, C, SL))
+    inputs = g.normal(size=(1, 12, C))
+    one, _ = oracle.conv_commit(pools=pools, inputs=inputs, token_start=[0], window_len=[5],
+                                accepted_len=[5], slot_table=[[2]], max_window=W)
+    a, _ = oracle.conv_commit(pools=pools, inputs=inputs, token_start=[0], window_len=[2],
+                              accepted_len=[2], slot_table=[[2]], max_window=W)
+    b, _ = oracle.conv_commit(pools=a, inputs=inputs, token_start=[2], window_len=[3],
+                              accepted_len=[3], slot_table=[[2]], max_window=W)
+    assert np.array_equal(one, b)
+    # align: block 4, checkpoint after 5 tokens (column 1), 5 accepted -> the
+    # state after token 8 goes to column 1, after token 10 to column 2
+    table = np.array([[-1, 4, 6, -1]], np.int32)
+    al, err = oracle.conv_commit(pools=pools, inputs=inputs, token_start=[0], window_len=[6],
+                                 accepted_len=[5], slot_table=table, seq_pos=[5], block_size=4,
+                                 max_window=W)
+    assert np.all(err == 0)
+    s3, _ = oracle.conv_commit(pools=pools, inputs=inputs, token_start=[0], window_len=[6],
+                               accepted_len=[3], slot_table=[[4]], max_window=W)
+    s5, _ = oracle.conv_commit(pools=pools, inputs=inputs, token_start=[0], window_len=[6],
+                               accepted_len=[5], slot_table=[[4]], max_window=W)
+    assert np.array_equal(al[0, 4], s3[0, 4]) and np.array_equal(al[0, 6], s5[0, 4])

@@ -94,3 +94,17 @@ def test_pack_inputs_keeps_values_and_layout(fused):
             assert got.shape == t.shape and got.stride() == stride and torch.equal(got, t)
             assert got.untyped_storage().data_ptr() == arena.untyped_storage().data_ptr()
     assert torch.equal(sb.slot_table, meta)
+
+
+def test_conv_state_generator_and_oracle_on_cpu():
+    sb = wl.long_ragged(L=2, batch=8, HK=2, HV=4, KV=16, num_slots=16, sentinel=False)
+    pools, inputs = wl.conv_state(sb, state_len=3)
+    C = 2 * sb.HK * sb.K + sb.HV * sb.V
+    assert pools[0].shape == (sb.num_slots, C, 3) and inputs[0].shape == (sb.T, C)
+    assert inputs[0].data_ptr() == sb.fused_qkv[0].data_ptr()      # fused rows reused
+    ref, err = oracle.conv_commit(pools=np.stack([p.double().numpy() for p in pools]),
+                                  inputs=np.stack([x.double().numpy() for x in inputs]),
+                                  token_start=sb.token_start, window_len=sb.window_len,
+                                  accepted_len=sb.accepted_len, slot_table=sb.slot_table,
+                                  max_window=sb.W)
+    assert np.all(err == 0)
