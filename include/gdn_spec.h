@@ -206,13 +206,16 @@ int gdn_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers,
  * written to the slots gdn_replay_commit writes for x = n (and, in align
  * mode, for each boundary).  Pure copies: results are bit-exact.
  *
- *   channels, state_len  C >= 1, 1 <= state_len <= 8; dtype: element type of
- *                  both the state and the inputs (F32 or BF16).
+ *   channels, state_len  C a multiple of 8, 1 <= state_len <= 8; dtype:
+ *                  element type of both the state and the inputs (F32 or
+ *                  BF16).
  *   conv_pools     device array [num_layers] of device pointers to
- *                  [num_slots][C][state_len] states, updated in place.
+ *                  [num_slots][C][state_len] states, 16-byte aligned,
+ *                  updated in place.
  *   conv_inputs    device array [num_layers] of device pointers to the
  *                  layer's convolution inputs, one row of C elements per
- *                  token row, rows input_row_stride elements apart.
+ *                  token row, rows input_row_stride elements apart (a
+ *                  multiple of 8); each pointer 16-byte aligned.
  *   token_start    [batch]: first token row of each request's window.
  *   layer_group / num_groups / slot_tables / group_stride as in
  *                  gdn_replay_commit_grouped (num_groups = 1 and layer_group

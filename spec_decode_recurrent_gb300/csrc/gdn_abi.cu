@@ -224,7 +224,7 @@ int gdn_conv_state_commit(int32_t num_layers, int32_t num_groups, const int32_t*
   if (block_size > 0 && !seq_pos) return GDN_ERR_NULL;
   if (num_layers < 1 || num_layers > 65535 || batch < 0 || batch > 65535 || num_slots < 0 ||
       num_tokens < 0 || num_groups < 1 || block_size < 0 || slot_table_stride < 1 ||
-      input_row_stride < channels)
+      input_row_stride < channels || channels % 8 != 0 || input_row_stride % 8 != 0)
     return GDN_ERR_INVALID;
   if (num_groups > 1 && group_stride < (int64_t)batch * slot_table_stride) return GDN_ERR_INVALID;
   gdn::ConvParams p;

@@ -11,22 +11,45 @@
 // written to the final slot and, in align mode, to every boundary slot.
 //
 // Pure data movement: every stored element is a copy of an input element,
-// so results are bit-exact by construction.  One thread per channel: it
-// loads its channel's whole checkpoint state into registers before writing
-// anything, so a boundary slot equal to the checkpoint slot cannot be read
-// after it has been overwritten.
+// so results are bit-exact by construction.  A thread loads its channels'
+// whole checkpoint state into registers before writing anything and then
+// shifts it token by token, so a boundary slot equal to the checkpoint slot
+// cannot be read after it has been overwritten.
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
 
 namespace gdn {
 
 constexpr int kConvThreads = 256;
-constexpr int kMaxConvState = 8;
 
-template <typename T>
+// 32-bit word k of a 16-byte chunk (k a compile-time constant after unrolling).
+__device__ __forceinline__ uint32_t chunk_word(const uint4& q, int k) {
+  return k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
+}
+// Element i of a chunk of 16-bit (B = 2) or 32-bit (B = 4) elements.
+template <int B>
+__device__ __forceinline__ uint32_t chunk_elem(const uint4& q, int i) {
+  if (B == 4) return chunk_word(q, i);
+  return (chunk_word(q, i >> 1) >> ((i & 1) * 16)) & 0xffffu;
+}
+template <int B, int NE>
+__device__ __forceinline__ uint4 make_chunk(const uint32_t (&e)[NE], int k) {
+  constexpr int E = 16 / B;
+  if (B == 4) return make_uint4(e[k * E], e[k * E + 1], e[k * E + 2], e[k * E + 3]);
+  return make_uint4(e[k * E] | (e[k * E + 1] << 16), e[k * E + 2] | (e[k * E + 3] << 16),
+                    e[k * E + 4] | (e[k * E + 5] << 16), e[k * E + 6] | (e[k * E + 7] << 16));
+}
+
+// A thread owns one group of E = 16 / B channels (B = element bytes): their
+// states are E * SL contiguous elements (SL 16-byte chunks) and each token
+// row gives one 16-byte chunk of their inputs, so every access is a full
+// 16 bytes.  Elements travel as raw bits in 32-bit registers.
+template <int B, int SL>
 __global__ void __launch_bounds__(kConvThreads) gdn_conv_commit_kernel(const ConvParams p) {
+  constexpr int E = 16 / B;   // channels per thread
+  constexpr int NE = E * SL;  // state elements per thread
   const int r = blockIdx.y, layer = blockIdx.z;
-  const int c = blockIdx.x * kConvThreads + threadIdx.x;
+  const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * E;
 
   const int g = p.layer_group ? p.layer_group[layer] : 0;
   const int32_t* trow = (g < 0 || g >= p.num_groups)
@@ -43,46 +66,64 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_commit_kernel(const Con
     if (p.err && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, plan.err);
     return;
   }
-  if (!plan.live || c >= p.C) return;
+  if (!plan.live || c0 >= p.C) return;
 
-  const int SL = p.SL;
-  T* pool = static_cast<T*>(p.pools[layer]);
-  const T* in = static_cast<const T*>(p.inputs[layer]);
-  const T* src = pool + ((size_t)plan.src * p.C + c) * SL;
-  T old[kMaxConvState];
+  unsigned char* pool = static_cast<unsigned char*>(p.pools[layer]);
+  const unsigned char* in = static_cast<const unsigned char*>(p.inputs[layer]);
+  // the checkpoint state of the group, element ch * SL + j, read before any
+  // write; then one shift per accepted token: drop the oldest entry of each
+  // channel and append the token's input
+  uint32_t st[NE];
+  {
+    const uint4* src =
+        reinterpret_cast<const uint4*>(pool + ((size_t)plan.src * p.C + c0) * SL * B);
 #pragma unroll
-  for (int j = 0; j < kMaxConvState; ++j)
-    if (j < SL) old[j] = src[j];
-
-  // sequence element i: i < SL from the checkpoint, else input row i - SL
-  auto element = [&](int i) -> T {
-    T v = old[0];
+    for (int k = 0; k < SL; ++k) {
+      const uint4 q = __ldcg(src + k);
 #pragma unroll
-    for (int j = 1; j < kMaxConvState; ++j)
-      if (i == j) v = old[j];
-    return i < SL ? v : in[(t0 + i - SL) * p.in_stride + c];
-  };
-  auto store_after = [&](int x, int slot) {
-    T* dst = pool + ((size_t)slot * p.C + c) * SL;
-    for (int j = 0; j < SL; ++j) dst[j] = element(x + j);
-  };
-  if (p.block_size > 0) {
-    for (int x = 1; x < plan.n; ++x) {
-      const long long pos = plan.p0 + x;
-      if (pos % p.block_size == 0)
-        store_after(x, slot_after(trow, p.table_stride, p.block_size, pos));
+      for (int i = 0; i < E; ++i) st[k * E + i] = chunk_elem<B>(q, i);
     }
   }
-  store_after(plan.n, plan.fin);
+  auto dst_of = [&](int slot) {
+    return reinterpret_cast<uint4*>(pool + ((size_t)slot * p.C + c0) * SL * B);
+  };
+  for (int t = 0; t < plan.n; ++t) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(in + ((t0 + t) * p.in_stride + c0) * B));
+#pragma unroll
+    for (int ch = 0; ch < E; ++ch) {
+#pragma unroll
+      for (int j = 0; j + 1 < SL; ++j) st[ch * SL + j] = st[ch * SL + j + 1];
+      st[ch * SL + SL - 1] = chunk_elem<B>(q, ch);
+    }
+    const long long pos = plan.p0 + t + 1;
+    const bool boundary = p.block_size > 0 && t + 1 < plan.n && pos % p.block_size == 0;
+    if (boundary || t + 1 == plan.n) {
+      uint4* dst = dst_of(boundary ? slot_after(trow, p.table_stride, p.block_size, pos)
+                                   : plan.fin);
+#pragma unroll
+      for (int k = 0; k < SL; ++k) __stcs(dst + k, make_chunk<B, NE>(st, k));
+    }
+  }
+}
+
+template <int B>
+static int launch_conv_t(const ConvParams& p, cudaStream_t stream) {
+  constexpr int E = 16 / B;
+  const int groups = p.C / E;
+  dim3 grid((groups + kConvThreads - 1) / kConvThreads, p.batch, p.num_layers);
+  switch (p.SL) {
+#define GDN_SL(N) \
+  case N: gdn_conv_commit_kernel<B, N><<<grid, kConvThreads, 0, stream>>>(p); break;
+    GDN_SL(1) GDN_SL(2) GDN_SL(3) GDN_SL(4) GDN_SL(5) GDN_SL(6) GDN_SL(7) GDN_SL(8)
+#undef GDN_SL
+    default: return GDN_ERR_UNSUPPORTED;
+  }
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 int launch_conv_commit(const ConvParams& p, int dtype, cudaStream_t stream) {
-  dim3 grid((p.C + kConvThreads - 1) / kConvThreads, p.batch, p.num_layers);
-  if (dtype == GDN_DTYPE_BF16)
-    gdn_conv_commit_kernel<unsigned short><<<grid, kConvThreads, 0, stream>>>(p);
-  else
-    gdn_conv_commit_kernel<unsigned int><<<grid, kConvThreads, 0, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  if (dtype == GDN_DTYPE_BF16) return launch_conv_t<2>(p, stream);
+  return launch_conv_t<4>(p, stream);
 }
 
 }  // namespace gdn

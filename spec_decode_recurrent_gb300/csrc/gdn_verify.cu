@@ -8,17 +8,14 @@
 // batches still fill 152 SMs, and a tile is wide enough that the per-token
 // staging -- key/query norms, gates -- is shared by many rows).  Rows of S
 // are independent given (khat, qhat, alpha, beta, v_i), so tiles never
-// communicate; the only reductions are over K, inside the K/32 lanes that
-// share a row, by warp shuffles.
+// communicate; the only reductions are over K, inside a group of K/16
+// lanes, by warp shuffles.
 //
-// Register layout of a tile, for K = 128: LPR = 4 lanes share one state row
-// and each lane holds 32 of its columns, as eight 4-column chunks at
-// columns 4 * (l + LPR * m), m = 0..7, kept as sixteen packed fp32 pairs;
-// for each chunk index a warp reads eight rows' 64-byte runs.  A warp covers
-// RPW = 8 rows; the row reductions take two xor-shuffle rounds.  The
-// normalised key and query stay in shared memory and are streamed through
-// the token's passes, which keeps a thread at ~80 registers (three CTAs per
-// SM).
+// Register layout of a tile, for K = 128: LPR = 8 lanes share one state row
+// and each lane holds 16 of its columns, as four 4-column chunks at columns
+// 4 * (l + LPR * m), m = 0..3, kept as eight packed fp32 pairs; a warp's
+// load of chunk m reads whole 128-byte lines.  A warp covers RPW = 32 / LPR
+// rows per row group and each thread keeps RPT row groups.
 //
 // Per token: H = alpha * S; both dot products are taken in one pass over H,
 // d = H khat and H qhat; then u = beta * (v - d), S = H + u khat^T and
@@ -37,13 +34,12 @@ namespace gdn {
 
 template <int K>
 struct VerifyTile {
-  static constexpr int CPL = K < 32 ? K : 32;   // columns per lane
-  static constexpr int LPR = K / CPL;           // lanes per state row (4 at K = 128)
-  static constexpr int NC = CPL / 4;            // 4-column chunks per lane
-  static constexpr int RPW = 32 / LPR;          // rows per warp
+  static constexpr int LPR = K / 16;              // lanes per state row
+  static constexpr int RPW = 32 / LPR;            // rows per warp per row group
+  static constexpr int RPT = (K == 128) ? 2 : 1;  // row groups per thread
   static constexpr int WARPS = 8;
   static constexpr int THREADS = 32 * WARPS;
-  static constexpr int VT = WARPS * RPW;        // state rows per CTA (64 at K = 128)
+  static constexpr int VT = WARPS * RPW * RPT;    // state rows per CTA
 };
 
 // Dynamic shared memory of one verify CTA, in floats.
@@ -53,10 +49,10 @@ __host__ __device__ constexpr int verify_smem_floats(int W) {
 }
 
 template <int K, typename QKV, typename ST, bool NATIVE, bool FULL>
-__global__ void __launch_bounds__(VerifyTile<K>::THREADS, 3)
+__global__ void __launch_bounds__(VerifyTile<K>::THREADS)
     gdn_verify_kernel(const VerifyParams p) {
   using Tile = VerifyTile<K>;
-  constexpr int LPR = Tile::LPR, RPW = Tile::RPW, NC = Tile::NC, VT = Tile::VT;
+  constexpr int LPR = Tile::LPR, RPW = Tile::RPW, RPT = Tile::RPT, VT = Tile::VT;
   extern __shared__ float smem[];
 
   const int tile = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
@@ -79,23 +75,28 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS, 3)
   if (src.slot < 0) return;  // null row or empty window: writes nothing
 
   const int hk = h / (p.HV / p.HK);
-  const int l = lane % LPR;   // column lane inside the row
-  const int row = tile * VT + warp * RPW + lane / LPR;
-  const bool row_ok = FULL || row < p.V;
+  const int l = lane % LPR;   // column lane inside the row group
+  const int lr = lane / LPR;  // row inside the warp's row group
 
   // ---- issue the checkpoint tile loads first; they stay in flight while
-  // ---- the token inputs are staged.  Chunk m holds columns
-  // ---- 4*(l + LPR*m) + {0..3}: s[2m] = +0,+1 and s[2m+1] = +2,+3.
+  // ---- the token inputs are staged.  Row group g holds columns
+  // ---- 4*(l + LPR*m) + {0..3}: s[g][2m] = +0,+1 and s[g][2m+1] = +2,+3.
   const ST* S0 = static_cast<const ST*>(p.pool) +
                  ((size_t)src.slot * p.HV + h) * (size_t)p.V * K;
-  f32x2 s[2 * NC];
-  if (row_ok) {
+  f32x2 s[RPT][8];
+  int rows[RPT];
 #pragma unroll
-    for (int m = 0; m < NC; ++m)
-      load_state_pairs(S0 + (size_t)row * K + 4 * (l + LPR * m), s[2 * m], s[2 * m + 1]);
-  } else {
+  for (int g = 0; g < RPT; ++g) {
+    rows[g] = tile * VT + (g * Tile::WARPS + warp) * RPW + lr;
+    if (FULL || rows[g] < p.V) {
 #pragma unroll
-    for (int j = 0; j < 2 * NC; ++j) s[j] = 0ull;
+      for (int m = 0; m < 4; ++m)
+        load_state_pairs(S0 + (size_t)rows[g] * K + 4 * (l + LPR * m), s[g][2 * m],
+                         s[g][2 * m + 1]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[g][j] = 0ull;
+    }
   }
 
   // ---- stage normalised keys / queries, their dot product, values and
@@ -155,8 +156,8 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS, 3)
   }
   // this tile's value rows of every token, all threads
   for (int i = tid; i < w * VT; i += Tile::THREADS) {
-    const int t = i / VT, vr = tile * VT + i % VT;
-    v_s[i] = (FULL || vr < p.V) ? load1(vb + (t0 + t) * p.v_stride + (size_t)h * p.V + vr) : 0.f;
+    const int t = i / VT, row = tile * VT + i % VT;
+    v_s[i] = (FULL || row < p.V) ? load1(vb + (t0 + t) * p.v_stride + (size_t)h * p.V + row) : 0.f;
   }
   __syncthreads();
 
@@ -167,69 +168,78 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS, 3)
   }
 
   // ---- output / record / snapshot cursors, advanced once per token
-  const bool writer = row_ok && l == 0;
-  float* optr = p.out + t0 * p.out_stride + (size_t)h * p.V + row;
-  float* uptr = NATIVE ? nullptr : p.rec_u + rec_base * p.V + row;
-  ST* sptr = NATIVE ? static_cast<ST*>(p.snaps) + ((size_t)r * p.W * p.HV + h) * (size_t)p.V * K +
-                          (size_t)row * K + 4 * l
-                    : nullptr;
+  const bool writer = (l == 0);
+  float* optr[RPT];
+  float* uptr[RPT];
+  ST* sptr[RPT];
+#pragma unroll
+  for (int g = 0; g < RPT; ++g) {
+    optr[g] = p.out + t0 * p.out_stride + (size_t)h * p.V + rows[g];
+    uptr[g] = NATIVE ? nullptr : p.rec_u + rec_base * p.V + rows[g];
+    sptr[g] = NATIVE ? static_cast<ST*>(p.snaps) + ((size_t)r * p.W * p.HV + h) * (size_t)p.V * K +
+                           (size_t)rows[g] * K + 4 * l
+                     : nullptr;
+  }
   const size_t snap_step = (size_t)p.HV * p.V * K;
-  const float* vrow = v_s + (row - tile * VT);
 
   // ---- the draft window, token by token, state in registers
   for (int t = 0; t < w; ++t) {
     const float be = be_s[t], kq = kq_s[t];
     const f32x2 al2 = pack2(al_s[t], al_s[t]);
-    const float* kt = kh_s + t * K + 4 * l;
-    const float* qt = qh_s + t * K + 4 * l;
-    // H = alpha * S
+    f32x2 kk[8], qq[8];
 #pragma unroll
-    for (int j = 0; j < 2 * NC; ++j) s[j] = mul2(s[j], al2);
-    // d = H khat and H qhat in one pass over the chunks: even and odd pair
-    // accumulators, combined pairwise, lanes summed, then the LPR lanes
-    f32x2 da, db, oa, ob;
+    for (int m = 0; m < 4; ++m) {
+      const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kh_s + t * K + 4 * (l + LPR * m));
+      const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(qh_s + t * K + 4 * (l + LPR * m));
+      kk[2 * m] = k4.x; kk[2 * m + 1] = k4.y;
+      qq[2 * m] = q4.x; qq[2 * m + 1] = q4.y;
+    }
 #pragma unroll
-    for (int m = 0; m < NC; ++m) {
-      const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kt + 4 * LPR * m);
-      const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(qt + 4 * LPR * m);
-      if (m == 0) {
-        da = mul2(s[0], k4.x); db = mul2(s[1], k4.y);
-        oa = mul2(s[0], q4.x); ob = mul2(s[1], q4.y);
-      } else {
-        da = fma2(s[2 * m], k4.x, da); db = fma2(s[2 * m + 1], k4.y, db);
-        oa = fma2(s[2 * m], q4.x, oa); ob = fma2(s[2 * m + 1], q4.y, ob);
+    for (int g = 0; g < RPT; ++g) {
+      // H = alpha * S
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], al2);
+      // d = H khat and H qhat in one pass: pair accumulators over pairs
+      // 0-3 and 4-7, combined pairwise, lanes summed, then the LPR lanes
+      f32x2 da = mul2(s[g][0], kk[0]), db = mul2(s[g][4], kk[4]);
+      f32x2 oa = mul2(s[g][0], qq[0]), ob = mul2(s[g][4], qq[4]);
+#pragma unroll
+      for (int j = 1; j < 4; ++j) {
+        da = fma2(s[g][j], kk[j], da);
+        db = fma2(s[g][4 + j], kk[4 + j], db);
+        oa = fma2(s[g][j], qq[j], oa);
+        ob = fma2(s[g][4 + j], qq[4 + j], ob);
       }
-    }
-    const float2 dd = unpack2(add2(da, db)), oo = unpack2(add2(oa, ob));
-    float d = __fadd_rn(dd.x, dd.y), o = __fadd_rn(oo.x, oo.y);
+      const float2 dd = unpack2(add2(da, db)), oo = unpack2(add2(oa, ob));
+      float d = __fadd_rn(dd.x, dd.y), o = __fadd_rn(oo.x, oo.y);
 #pragma unroll
-    for (int off = LPR / 2; off >= 1; off >>= 1) {
-      d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, off));
-      o = __fadd_rn(o, __shfl_xor_sync(0xffffffffu, o, off));
-    }
-    const float vi = row_ok ? vrow[t * VT] : 0.f;
-    const float u = __fmul_rn(be, __fsub_rn(vi, d));
-    o = __fmaf_rn(u, kq, o);
-    // S = H + u khat^T
-    const f32x2 u2 = pack2(u, u);
+      for (int off = LPR / 2; off >= 1; off >>= 1) {
+        d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, off));
+        o = __fadd_rn(o, __shfl_xor_sync(0xffffffffu, o, off));
+      }
+      const float vi = (FULL || rows[g] < p.V) ? v_s[t * VT + rows[g] - tile * VT] : 0.f;
+      const float u = __fmul_rn(be, __fsub_rn(vi, d));
+      o = __fmaf_rn(u, kq, o);
+      // S = H + u khat^T
+      const f32x2 u2 = pack2(u, u);
 #pragma unroll
-    for (int m = 0; m < NC; ++m) {
-      const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kt + 4 * LPR * m);
-      s[2 * m] = fma2(u2, k4.x, s[2 * m]);
-      s[2 * m + 1] = fma2(u2, k4.y, s[2 * m + 1]);
-    }
+      for (int j = 0; j < 8; ++j) s[g][j] = fma2(u2, kk[j], s[g][j]);
 
-    if (writer) {
-      *optr = o;
-      if (!NATIVE) *uptr = u;
-    }
-    if (NATIVE && row_ok) {
+      if (FULL || rows[g] < p.V) {
+        if (writer) {
+          *optr[g] = o;
+          if (!NATIVE) *uptr[g] = u;
+        }
+        if (NATIVE) {
 #pragma unroll
-      for (int m = 0; m < NC; ++m) store_state_pairs(sptr + 4 * LPR * m, s[2 * m], s[2 * m + 1]);
+          for (int m = 0; m < 4; ++m)
+            store_state_pairs(sptr[g] + 4 * LPR * m, s[g][2 * m], s[g][2 * m + 1]);
+        }
+      }
+      optr[g] += p.out_stride;
+      if (!NATIVE) uptr[g] += p.V;
+      if (NATIVE) sptr[g] += snap_step;
     }
-    optr += p.out_stride;
-    if (!NATIVE) uptr += p.V;
-    if (NATIVE) sptr += snap_step;
   }
 }
 
