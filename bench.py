@@ -363,36 +363,104 @@ def run_e2e(args, sb, bufs, graph, stream, arena):
     """The same step through the public API with host buffers: every step
     copies all of its inputs (q/k/v, gates, row metadata of every layer)
     from pinned host memory in one copy, runs, and reads back every layer's
-    output and the error word."""
+    output and the error word.  Measured twice: serially (copy in, compute,
+    copy out, one after the other) and pipelined, as a serving loop runs it,
+    with two input arenas and two output sets so that step i+1's inputs and
+    step i-1's outputs cross the bus on their own streams while step i
+    computes.  `value` is the pipelined figure; every step still moves its
+    own bytes inside the timed region."""
+    import dataclasses
+    # second arena, outputs and verify graph (they bake in their addresses);
+    # the state pools are shared, as they are in a serving engine
+    sb2 = dataclasses.replace(sb, q=list(sb.q), k=list(sb.k), v=list(sb.v), a=list(sb.a),
+                              b=list(sb.b),
+                              fused_qkv=None if sb.fused_qkv is None else list(sb.fused_qkv))
+    arena2 = step.pack_inputs(sb2)
+    bufs2 = step.StepBuffers(sb2)
+    step.verify_all(sb2, bufs2)
+    torch.cuda.synchronize()
+    graph2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph2):
+        step.verify_all(sb2, bufs2)
+    torch.cuda.synchronize()
+    sets = [(sb, bufs, graph, arena), (sb2, bufs2, graph2, arena2)]
     host_in = arena.cpu().pin_memory()
-    host_out = torch.empty(bufs.out_all.shape, dtype=torch.float32, pin_memory=True)
-    host_err = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    host_out = [torch.empty(bufs.out_all.shape, dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    host_err = [torch.empty(1, dtype=torch.int32, pin_memory=True) for _ in range(2)]
     bi = host_in.numel()
-    bo = host_out.numel() * 4 + 4
+    bo = host_out[0].numel() * 4 + 4
+    E = max(2, args.e2e_steps)
 
-    def one():
-        arena.copy_(host_in, non_blocking=True)
-        graph.replay()
-        step.commit(sb, bufs)
-        host_out.copy_(bufs.out_all, non_blocking=True)
-        host_err.copy_(bufs.err, non_blocking=True)
+    def serial(n):
+        for _ in range(n):
+            arena.copy_(host_in, non_blocking=True)
+            graph.replay()
+            step.commit(sb, bufs)
+            host_out[0].copy_(bufs.out_all, non_blocking=True)
+            host_err[0].copy_(bufs.err, non_blocking=True)
 
-    for _ in range(3):
-        one()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+
+    def pipelined(n, t0=None, t1=None):
+        ready, done, drained = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        used = [False, False]
+        if t0 is not None:
+            t0.record(h2d)
+
+        def copy_in(i):
+            s_ = i % 2
+            with torch.cuda.stream(h2d):
+                if used[s_]:
+                    h2d.wait_event(done[s_])        # the step that last read this arena is over
+                sets[s_][3].copy_(host_in, non_blocking=True)
+                ready[s_].record(h2d)
+
+        copy_in(0)
+        for i in range(n):
+            s_ = i % 2
+            sbi, bfi, gi, _ = sets[s_]
+            if i + 1 < n:
+                copy_in(i + 1)
+            stream.wait_event(ready[s_])
+            if used[s_]:
+                stream.wait_event(drained[s_])      # its outputs of two steps ago are read back
+            gi.replay()
+            step.commit(sbi, bfi)
+            done[s_].record(stream)
+            used[s_] = True
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(done[s_])
+                host_out[s_].copy_(bfi.out_all, non_blocking=True)
+                host_err[s_].copy_(bfi.err, non_blocking=True)
+                drained[s_].record(d2h)
+        if t1 is not None:
+            for e_ in (done[(n - 1) % 2], drained[0], drained[1]):
+                d2h.wait_event(e_)
+            t1.record(d2h)
+
+    serial(3)
+    pipelined(4)
     torch.cuda.synchronize()
     dist.barrier()
-    E = max(1, args.e2e_steps)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(E):
-        one()
+    serial(E)
     b.record(stream)
     torch.cuda.synchronize()
-    ms = dist.max_over_ranks(a.elapsed_time(b), torch.cuda.current_device()) / E
-    return {"value": round(ms * 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo, "steps": E,
+    serial_ms = dist.max_over_ranks(a.elapsed_time(b), torch.cuda.current_device()) / E
+    c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pipelined(E, c, d)
+    torch.cuda.synchronize()
+    pipe_ms = dist.max_over_ranks(c.elapsed_time(d), torch.cuda.current_device()) / E
+    assert int(host_err[0].item()) == 0 and int(host_err[1].item()) == 0
+    del sb2, bufs2, graph2, arena2
+    return {"value": round(pipe_ms * 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "steps": E, "serial_value": round(serial_ms * 1e3, 3),
             "path": "one pinned host -> device copy of every input of the step, verify graph + "
-                    "commit call, one device -> host copy of every layer's output, error word"}
+                    "commit call, one device -> host copy of every layer's output and the error "
+                    "word; value: copies of neighbouring steps overlap the compute (two arenas, "
+                    "copy streams); serial_value: copy, compute, copy in sequence"}
 
 
 def run_grouped(args):

@@ -1,15 +1,14 @@
 // gdn_verify.cu -- speculative verify and native per-draft snapshot kernels.
 //
-// One CTA of 8 warps owns a tile of VT state rows (64 for K = 128) of one
+// One CTA of 4 warps owns a tile of VT state rows (32 for K = 128) of one
 // (request row, value head) and runs the whole draft window over it with
 // the tile held in registers (tokenspeed PR "feat: add Qwen3.5 GDN
-// ReplaySSM", Summary and Implementation: a cooperative multi-warp CTA per
-// 128x128 state head; here a head is split into V tiles so that small
-// batches still fill 152 SMs, and a tile is wide enough that the per-token
-// staging -- key/query norms, gates -- is shared by many rows).  Rows of S
-// are independent given (khat, qhat, alpha, beta, v_i), so tiles never
-// communicate; the only reductions are over K, inside a group of K/16
-// lanes, by warp shuffles.
+// ReplaySSM", Summary and Implementation: a cooperative 4-warp CTA per
+// 128x128 state head; here a head is further split into 32-row tiles, so
+// that small batches still fill 152 SMs and seven small CTAs per SM hide
+// each other's load and staging latency).  Rows of S are independent given
+// (khat, qhat, alpha, beta, v_i), so tiles never communicate; the only
+// reductions are over K, inside a group of K/16 lanes, by warp shuffles.
 //
 // Register layout of a tile, for K = 128: LPR = 8 lanes share one state row
 // and each lane holds 16 of its columns, as four 4-column chunks at columns
@@ -37,7 +36,7 @@ struct VerifyTile {
   static constexpr int LPR = K / 16;              // lanes per state row
   static constexpr int RPW = 32 / LPR;            // rows per warp per row group
   static constexpr int RPT = (K == 128) ? 2 : 1;  // row groups per thread
-  static constexpr int WARPS = 8;
+  static constexpr int WARPS = 4;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int VT = WARPS * RPW * RPT;    // state rows per CTA
 };

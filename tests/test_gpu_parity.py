@@ -229,3 +229,33 @@ def test_align_commit_repeatable_bitwise():
             for a, b in zip(results, now):
                 assert torch.equal(a, b)
     assert int(bufs.err.item()) == 0
+
+
+def test_graph_captured_step_matches_eager_bitwise():
+    # The benchmark replays the per-layer verify calls from a CUDA graph
+    # captured through the C ABI; replay must give the eager results bit
+    # for bit (same kernels, same launch configuration).
+    sb = wl.custom(device="cuda", sentinel=False, HK=2, HV=4, K=128, V=128, W=4, L=3,
+                   windows=[4, 3, 0, 4], accepted=[2, 3, 0, 4])
+    before = [p.clone() for p in sb.pools]
+    eager = step.StepBuffers(sb, fill=float("nan"))
+    step.verify_all(sb, eager)
+    step.commit(sb, eager)
+    torch.cuda.synchronize()
+    eager_pools = [p.clone() for p in sb.pools]
+    for p, b in zip(sb.pools, before):
+        p.copy_(b)
+    bufs = step.StepBuffers(sb, fill=float("nan"))
+    step.verify_all(sb, bufs)                     # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step.verify_all(sb, bufs)
+    bufs.out_all.fill_(float("nan"))
+    g.replay()
+    step.commit(sb, bufs)
+    torch.cuda.synchronize()
+    for l in range(sb.L):
+        assert torch.equal(bufs.out[l].view(torch.int32), eager.out[l].view(torch.int32))
+        assert torch.equal(bufs.rec_u[l].view(torch.int32), eager.rec_u[l].view(torch.int32))
+        assert torch.equal(sb.pools[l].view(torch.int32), eager_pools[l].view(torch.int32))
