@@ -43,6 +43,8 @@ DESCR = {
                  "bf16 q/k/v, fp32 [V,K] state, slots a random permutation of a 256-slot pool, seed 2",
     "layer": "1 GDN layer at serving shape, batch 16, HK=16 HV=32 K=V=128, window 4, "
              "accepted uniform 1..4, bf16 q/k/v, fp32 state, seed 1",
+    "mtp5": "all_layer shapes with window 6 (MTP 5) and accepted lengths drawn from measured "
+            "per-position acceptance .856/.694/.558/.457/.376 (mean 3.941), seed 5",
     "long_ragged": "36 GDN layers, batch 256, window 6 mixed with ragged 4/1/3, permuted "
                    "non-contiguous rows, strided fused q/k/v, gates U(-20,20), 512-slot pools, seed 30",
     "align": "36 GDN layers, batch 128, window 4, align mode with block size 4, boundary "
@@ -76,9 +78,12 @@ def make_workload(name, device, rank, state_dtype, layers=None):
     kw = dict(device=device, sentinel=False)
     if layers is not None:
         kw["L"] = layers
-    base = {"all_layer": 2, "layer": 1, "long_ragged": 30, "align": 4}[name]
+    base = {"all_layer": 2, "layer": 1, "long_ragged": 30, "align": 4, "mtp5": 5}[name]
     kw["seed"] = dist.replica_seed(base, rank)
-    if name in ("all_layer", "align") and state_dtype == torch.bfloat16:
+    if state_dtype == torch.bfloat16:
+        import inspect
+        if "state_dtype" not in inspect.signature(fn).parameters:
+            raise SystemExit(f"workload {name} has no bf16-state form")
         kw["state_dtype"] = state_dtype
     return fn(**kw)
 

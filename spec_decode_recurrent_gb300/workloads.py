@@ -218,6 +218,39 @@ def all_layer(device="cpu", sentinel=True, seed=2, L=36, batch=64, pad_rows=8, H
                  sentinel=sentinel)
 
 
+# Per-position acceptance rates of a five-draft (window 6) run, P(n >= 1 + i)
+# for i = 1..5, as measured in the review thread of vLLM PR "[Spec Decode]
+# [Qwen4Exp] RecoverSSM for Qwen GDN and the PLE short conv" (the MTP 5 run's
+# accept-length note); the mean accepted length they imply is 3.941.
+MTP5_ACCEPT = (0.856, 0.694, 0.558, 0.457, 0.376)
+
+
+def accepted_from_profile(gen, profile, n):
+    """n accepted lengths with P(len >= 1 + i) = profile[i - 1]: one uniform
+    u per row, len = 1 + #{i : u < profile[i - 1]} (the rates decrease, so
+    u < profile[i] implies u < every earlier rate)."""
+    u = torch.rand(n, generator=gen, dtype=torch.float64).tolist()
+    return [1 + sum(1 for p in profile if x < p) for x in u]
+
+
+def mtp5(device="cpu", sentinel=True, seed=5, L=36, batch=64, pad_rows=8, HK=16, HV=32,
+         KV=128, num_slots=256, state_dtype=F32):
+    """The all_layer shapes with window 6 (five drafts) and accepted lengths
+    drawn from the measured per-position acceptance rates (MTP5_ACCEPT)."""
+    cpu = _gen(seed, "cpu")
+    live = batch - pad_rows
+    window = 1 + len(MTP5_ACCEPT)
+    windows = [window] * live + [0] * pad_rows
+    accepted = accepted_from_profile(cpu, MTP5_ACCEPT, live) + [0] * pad_rows
+    perm = torch.randperm(num_slots, generator=cpu).tolist()
+    slots = [[perm[r]] for r in range(live)] + [[-1]] * pad_rows
+    gen = _gen(seed, device)
+    return _make("mtp5", HK=HK, HV=HV, K=KV, V=KV, W=window, L=L, windows=windows,
+                 accepted=accepted, num_slots=num_slots, slots_for_row=slots,
+                 qkv_dtype=BF16, state_dtype=state_dtype, gen=gen, device=device,
+                 sentinel=sentinel)
+
+
 def long_ragged(device="cpu", sentinel=True, seed=30, L=36, batch=256, HK=16, HV=32, KV=128,
                 num_slots=512, window=6):
     """Long drafts and ragged windows: half the rows use the full window, the
@@ -278,6 +311,7 @@ WORKLOADS = {
     "tiny": tiny,
     "layer": layer,
     "all_layer": all_layer,
+    "mtp5": mtp5,
     "long_ragged": long_ragged,
     "align": align,
 }

@@ -95,6 +95,7 @@ def test_small_step_full_oracle(name):
 FULL = {
     "layer": lambda: wl.layer(device="cuda"),
     "all_layer": lambda: wl.all_layer(device="cuda"),
+    "mtp5": lambda: wl.mtp5(device="cuda"),
     "long_ragged_seed30": lambda: wl.long_ragged(device="cuda", seed=30),
     "long_ragged_seed31": lambda: wl.long_ragged(device="cuda", seed=31),
     "long_ragged_seed32": lambda: wl.long_ragged(device="cuda", seed=32),

@@ -44,7 +44,8 @@ def test_named_workloads_generate_small():
                wl.all_layer(L=2, batch=10, pad_rows=2, HK=2, HV=4, KV=16, num_slots=16),
                wl.long_ragged(L=2, batch=12, HK=2, HV=4, KV=16, num_slots=24),
                wl.align(L=2, batch=16, HK=2, HV=4, KV=16, num_slots=40),
-               wl.align(L=1, batch=16, HK=2, HV=4, KV=16, num_slots=40, state_dtype=wl.BF16)):
+               wl.align(L=1, batch=16, HK=2, HV=4, KV=16, num_slots=40, state_dtype=wl.BF16),
+               wl.mtp5(L=2, batch=12, pad_rows=2, HK=2, HV=4, KV=16, num_slots=24)):
         _check_layout(sb)
         assert roofline.commit_bytes(sb) > 0 and roofline.verify_bytes_per_layer(sb) > 0
 
@@ -108,3 +109,23 @@ def test_conv_state_generator_and_oracle_on_cpu():
                                   accepted_len=sb.accepted_len, slot_table=sb.slot_table,
                                   max_window=sb.W)
     assert np.all(err == 0)
+
+
+def test_mtp5_acceptance_profile_matches_the_measured_rates():
+    # the rates imply the mean accepted length printed beside them (3.941)
+    assert abs(1 + sum(wl.MTP5_ACCEPT) - 3.941) < 1e-9
+    n = 200_000
+    lens = np.array(wl.accepted_from_profile(torch.Generator().manual_seed(0), wl.MTP5_ACCEPT, n))
+    assert lens.min() >= 1 and lens.max() <= 6
+    for i, p in enumerate(wl.MTP5_ACCEPT, start=1):
+        sigma = (p * (1 - p) / n) ** 0.5
+        assert abs((lens >= 1 + i).mean() - p) < 5 * sigma, (i, (lens >= 1 + i).mean(), p)
+    assert abs(lens.mean() - 3.941) < 0.02
+    sb = wl.mtp5(L=1, batch=64, pad_rows=8, HK=2, HV=4, KV=16, num_slots=128)
+    live = sb.window_len > 0
+    assert int(live.sum()) == 56 and sb.W == 6
+    assert bool((sb.window_len[live] == 6).all())
+    acc = sb.accepted_len[live]
+    assert bool((acc >= 1).all() and (acc <= 6).all())
+    assert bool((sb.accepted_len[~live] == 0).all())
+
