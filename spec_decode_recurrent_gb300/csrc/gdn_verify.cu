@@ -1,14 +1,18 @@
 // gdn_verify.cu -- speculative verify and native per-draft snapshot kernels.
 //
-// One CTA of 4 warps owns a tile of VT state rows (32 for K = 128) of one
-// (request row, value head) and runs the whole draft window over it with
-// the tile held in registers (tokenspeed PR "feat: add Qwen3.5 GDN
-// ReplaySSM", Summary and Implementation: a cooperative 4-warp CTA per
-// 128x128 state head; here a head is further split into 32-row tiles, so
-// that small batches still fill 152 SMs and seven small CTAs per SM hide
-// each other's load and staging latency).  Rows of S are independent given
-// (khat, qhat, alpha, beta, v_i), so tiles never communicate; the only
-// reductions are over K, inside a group of K/16 lanes, by warp shuffles.
+// One CTA of 4 warps runs the whole draft window over up to four tiles of VT
+// state rows (32 for K = 128) of one (request row, value head), one tile
+// after another, with the tile held in registers (tokenspeed PR "feat: add
+// Qwen3.5 GDN ReplaySSM", Summary and Implementation: a cooperative 4-warp
+// CTA per 128x128 state head).  The window's normalised keys and queries,
+// gates and values are staged once per CTA for all of its tiles: that
+// staging and the row plan cost as many instructions as the recurrence of
+// one tile, so a head run as four separate tile CTAs paid them four times.
+// The tile buffer stays single (72 registers, seven CTAs per SM): the CTAs
+// of one SM hide each other's tile loads better than a second register or
+// shared-memory buffer would.  Rows of S are independent given (khat, qhat,
+// alpha, beta, v_i), so tiles never communicate; the only reductions are
+// over K, inside a group of K/16 lanes, by warp shuffles.
 //
 // Register layout of a tile, for K = 128: LPR = 8 lanes share one state row
 // and each lane holds 16 of its columns, as four 4-column chunks at columns
@@ -24,8 +28,9 @@
 // VERIFY mode writes o_t and the replay record (u_t, khat_t, alpha_t) and no
 // state (vLLM PR "[Spec Decode][Qwen4Exp] RecoverSSM for Qwen GDN and the
 // PLE short conv", Purpose).  NATIVE mode writes o_t and the full state after
-// every token instead.  Both run the identical arithmetic, so their outputs
-// agree bit for bit, and the state update is the commit's fold.
+// every token instead, one tile per CTA.  Both run the identical per-token
+// arithmetic on every row, so their outputs agree bit for bit however the
+// tiles are grouped into CTAs, and the state update is the commit's fold.
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
 
@@ -38,24 +43,134 @@ struct VerifyTile {
   static constexpr int RPT = (K == 128) ? 2 : 1;  // row groups per thread
   static constexpr int WARPS = 4;
   static constexpr int THREADS = 32 * WARPS;
-  static constexpr int VT = WARPS * RPW * RPT;    // state rows per CTA
+  static constexpr int VT = WARPS * RPW * RPT;    // state rows per tile
+  static constexpr int MIN_CTAS = 7;              // CTAs per SM the registers must allow
 };
 
-// Dynamic shared memory of one verify CTA, in floats.
+// Dynamic shared memory of one verify CTA covering NS tiles, in floats.
 template <int K>
-__host__ __device__ constexpr int verify_smem_floats(int W) {
-  return W * (2 * K + VerifyTile<K>::VT + 3);
+__host__ __device__ constexpr int verify_smem_floats(int W, int NS) {
+  return W * (2 * K + NS * VerifyTile<K>::VT + 3);
 }
 
-template <int K, typename QKV, typename ST, bool NATIVE, bool FULL>
-__global__ void __launch_bounds__(VerifyTile<K>::THREADS)
-    gdn_verify_kernel(const VerifyParams p) {
+// Checkpoint rows of one tile into a register buffer (zeros past V).
+template <int K, typename ST, bool FULL>
+__device__ __forceinline__ void load_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], const ST* S0, int tile,
+                                          int V, int warp, int l, int lr) {
+  using Tile = VerifyTile<K>;
+#pragma unroll
+  for (int g = 0; g < Tile::RPT; ++g) {
+    const int row = tile * Tile::VT + (g * Tile::WARPS + warp) * Tile::RPW + lr;
+    if (FULL || row < V) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        load_state_pairs(S0 + (size_t)row * K + 4 * (l + Tile::LPR * m), s[g][2 * m], s[g][2 * m + 1]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[g][j] = 0ull;
+    }
+  }
+}
+
+// The draft window over one tile whose state is in s.  vt_off: this tile's
+// first row inside the CTA's staged value rows.
+template <int K, typename ST, bool NATIVE, bool FULL>
+__device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], const VerifyParams& p,
+                                         int tile, int h, int r, int w, long long t0, int vt_off,
+                                         int vrow_stride, const float* kh_s, const float* qh_s,
+                                         const float* v_s, const float* al_s, const float* be_s,
+                                         const float* kq_s, int warp, int l, int lr) {
   using Tile = VerifyTile<K>;
   constexpr int LPR = Tile::LPR, RPW = Tile::RPW, RPT = Tile::RPT, VT = Tile::VT;
+  const size_t rec_base = ((size_t)r * p.HV + h) * p.W;
+  const bool writer = (l == 0);
+  int rows[RPT];
+  float* optr[RPT];
+  float* uptr[RPT];
+  ST* sptr[RPT];
+#pragma unroll
+  for (int g = 0; g < RPT; ++g) {
+    rows[g] = tile * VT + (g * Tile::WARPS + warp) * RPW + lr;
+    optr[g] = p.out + t0 * p.out_stride + (size_t)h * p.V + rows[g];
+    uptr[g] = NATIVE ? nullptr : p.rec_u + rec_base * p.V + rows[g];
+    sptr[g] = NATIVE ? static_cast<ST*>(p.snaps) + ((size_t)r * p.W * p.HV + h) * (size_t)p.V * K +
+                           (size_t)rows[g] * K + 4 * l
+                     : nullptr;
+  }
+  const size_t snap_step = (size_t)p.HV * p.V * K;
+  // ---- the draft window, token by token, state in registers
+  for (int t = 0; t < w; ++t) {
+    const float be = be_s[t], kq = kq_s[t];
+    const f32x2 al2 = pack2(al_s[t], al_s[t]);
+    f32x2 kk[8], qq[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kh_s + t * K + 4 * (l + LPR * m));
+      const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(qh_s + t * K + 4 * (l + LPR * m));
+      kk[2 * m] = k4.x; kk[2 * m + 1] = k4.y;
+      qq[2 * m] = q4.x; qq[2 * m + 1] = q4.y;
+    }
+#pragma unroll
+    for (int g = 0; g < RPT; ++g) {
+      // H = alpha * S
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], al2);
+      // d = H khat and H qhat in one pass: pair accumulators over pairs
+      // 0-3 and 4-7, combined pairwise, lanes summed, then the LPR lanes
+      f32x2 da = mul2(s[g][0], kk[0]), db = mul2(s[g][4], kk[4]);
+      f32x2 oa = mul2(s[g][0], qq[0]), ob = mul2(s[g][4], qq[4]);
+#pragma unroll
+      for (int j = 1; j < 4; ++j) {
+        da = fma2(s[g][j], kk[j], da);
+        db = fma2(s[g][4 + j], kk[4 + j], db);
+        oa = fma2(s[g][j], qq[j], oa);
+        ob = fma2(s[g][4 + j], qq[4 + j], ob);
+      }
+      const float2 dd = unpack2(add2(da, db)), oo = unpack2(add2(oa, ob));
+      float d = __fadd_rn(dd.x, dd.y), o = __fadd_rn(oo.x, oo.y);
+#pragma unroll
+      for (int off = LPR / 2; off >= 1; off >>= 1) {
+        d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, off));
+        o = __fadd_rn(o, __shfl_xor_sync(0xffffffffu, o, off));
+      }
+      const float vi = (FULL || rows[g] < p.V) ? v_s[t * vrow_stride + vt_off + rows[g] - tile * VT] : 0.f;
+      const float u = __fmul_rn(be, __fsub_rn(vi, d));
+      o = __fmaf_rn(u, kq, o);
+      // S = H + u khat^T
+      const f32x2 u2 = pack2(u, u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[g][j] = fma2(u2, kk[j], s[g][j]);
+      if (FULL || rows[g] < p.V) {
+        if (writer) {
+          *optr[g] = o;
+          if (!NATIVE) *uptr[g] = u;
+        }
+        if (NATIVE) {
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            store_state_pairs(sptr[g] + 4 * LPR * m, s[g][2 * m], s[g][2 * m + 1]);
+        }
+      }
+      optr[g] += p.out_stride;
+      if (!NATIVE) uptr[g] += p.V;
+      if (NATIVE) sptr[g] += snap_step;
+    }
+  }
+}
+
+// One CTA runs NS consecutive tiles of one (request row, value head): the
+// window's keys, queries, gates and values are staged once for all of them,
+// then each tile's checkpoint rows are loaded and its window run in turn.
+template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS>
+__global__ void __launch_bounds__(VerifyTile<K>::THREADS, VerifyTile<K>::MIN_CTAS)
+    gdn_verify_kernel(const VerifyParams p) {
+  using Tile = VerifyTile<K>;
+  constexpr int LPR = Tile::LPR, RPT = Tile::RPT, VT = Tile::VT;
   extern __shared__ float smem[];
 
-  const int tile = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
+  const int span = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile0 = span * NS;  // first tile of this CTA
 
   // ---- row plan: identical checks in every CTA of the row
   const int w = p.window_len[r];
@@ -68,7 +183,7 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
     if (t0 < 0 || t0 + w > p.num_tokens) src.err = GDN_ROW_ERR_TOKENS;
   }
   if (src.err) {
-    if (p.err && tid == 0 && tile == 0 && h == 0) atomicOr(p.err, src.err);
+    if (p.err && tid == 0 && span == 0 && h == 0) atomicOr(p.err, src.err);
     return;
   }
   if (src.slot < 0) return;  // null row or empty window: writes nothing
@@ -77,33 +192,20 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
   const int l = lane % LPR;   // column lane inside the row group
   const int lr = lane / LPR;  // row inside the warp's row group
 
-  // ---- issue the checkpoint tile loads first; they stay in flight while
-  // ---- the token inputs are staged.  Row group g holds columns
+  // ---- the first tile's checkpoint loads go out first; they stay in flight
+  // ---- while the window's inputs are staged.  Row group g holds columns
   // ---- 4*(l + LPR*m) + {0..3}: s[g][2m] = +0,+1 and s[g][2m+1] = +2,+3.
-  const ST* S0 = static_cast<const ST*>(p.pool) +
-                 ((size_t)src.slot * p.HV + h) * (size_t)p.V * K;
+  const ST* S0 = static_cast<const ST*>(p.pool) + ((size_t)src.slot * p.HV + h) * (size_t)p.V * K;
   f32x2 s[RPT][8];
-  int rows[RPT];
-#pragma unroll
-  for (int g = 0; g < RPT; ++g) {
-    rows[g] = tile * VT + (g * Tile::WARPS + warp) * RPW + lr;
-    if (FULL || rows[g] < p.V) {
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        load_state_pairs(S0 + (size_t)rows[g] * K + 4 * (l + LPR * m), s[g][2 * m],
-                         s[g][2 * m + 1]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s[g][j] = 0ull;
-    }
-  }
+  load_tile<K, ST, FULL>(s, S0, tile0, p.V, warp, l, lr);
 
-  // ---- stage normalised keys / queries, their dot product, values and
-  // ---- gates of the whole window in shared memory
+  // ---- stage normalised keys / queries, their dot product, the gates and
+  // ---- the value rows of all NS tiles for the whole window in shared memory
+  constexpr int SV = NS * VT;           // staged value rows
   float* kh_s = smem;                   // [W][K]
   float* qh_s = kh_s + p.W * K;         // [W][K]
-  float* v_s = qh_s + p.W * K;          // [W][VT]
-  float* al_s = v_s + p.W * VT;         // [W]
+  float* v_s = qh_s + p.W * K;          // [W][SV]
+  float* al_s = v_s + p.W * SV;         // [W]
   float* be_s = al_s + p.W;             // [W]
   float* kq_s = be_s + p.W;             // [W]
   const QKV* qb = static_cast<const QKV*>(p.q);
@@ -153,105 +255,57 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS)
     al_s[lane] = gate_decay(p.a[gi], p.A_log[h], p.dt_bias[h]);
     be_s[lane] = gate_beta(p.b[gi]);
   }
-  // this tile's value rows of every token, all threads
-  for (int i = tid; i < w * VT; i += Tile::THREADS) {
-    const int t = i / VT, row = tile * VT + i % VT;
+  // the value rows of this CTA's tiles, every token, all threads
+  for (int i = tid; i < w * SV; i += Tile::THREADS) {
+    const int t = i / SV, row = tile0 * VT + i % SV;
     v_s[i] = (FULL || row < p.V) ? load1(vb + (t0 + t) * p.v_stride + (size_t)h * p.V + row) : 0.f;
   }
   __syncthreads();
 
   const size_t rec_base = ((size_t)r * p.HV + h) * p.W;  // record position 0
-  if (!NATIVE && tile == 0) {
+  if (!NATIVE && span == 0) {
     for (int i = tid; i < w * K; i += Tile::THREADS) p.rec_k[rec_base * K + i] = kh_s[i];
     if (tid < w) p.rec_g[rec_base + tid] = al_s[tid];
   }
 
-  // ---- output / record / snapshot cursors, advanced once per token
-  const bool writer = (l == 0);
-  float* optr[RPT];
-  float* uptr[RPT];
-  ST* sptr[RPT];
-#pragma unroll
-  for (int g = 0; g < RPT; ++g) {
-    optr[g] = p.out + t0 * p.out_stride + (size_t)h * p.V + rows[g];
-    uptr[g] = NATIVE ? nullptr : p.rec_u + rec_base * p.V + rows[g];
-    sptr[g] = NATIVE ? static_cast<ST*>(p.snaps) + ((size_t)r * p.W * p.HV + h) * (size_t)p.V * K +
-                           (size_t)rows[g] * K + 4 * l
-                     : nullptr;
-  }
-  const size_t snap_step = (size_t)p.HV * p.V * K;
-
-  // ---- the draft window, token by token, state in registers
-  for (int t = 0; t < w; ++t) {
-    const float be = be_s[t], kq = kq_s[t];
-    const f32x2 al2 = pack2(al_s[t], al_s[t]);
-    f32x2 kk[8], qq[8];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kh_s + t * K + 4 * (l + LPR * m));
-      const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(qh_s + t * K + 4 * (l + LPR * m));
-      kk[2 * m] = k4.x; kk[2 * m + 1] = k4.y;
-      qq[2 * m] = q4.x; qq[2 * m + 1] = q4.y;
-    }
-#pragma unroll
-    for (int g = 0; g < RPT; ++g) {
-      // H = alpha * S
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], al2);
-      // d = H khat and H qhat in one pass: pair accumulators over pairs
-      // 0-3 and 4-7, combined pairwise, lanes summed, then the LPR lanes
-      f32x2 da = mul2(s[g][0], kk[0]), db = mul2(s[g][4], kk[4]);
-      f32x2 oa = mul2(s[g][0], qq[0]), ob = mul2(s[g][4], qq[4]);
-#pragma unroll
-      for (int j = 1; j < 4; ++j) {
-        da = fma2(s[g][j], kk[j], da);
-        db = fma2(s[g][4 + j], kk[4 + j], db);
-        oa = fma2(s[g][j], qq[j], oa);
-        ob = fma2(s[g][4 + j], qq[4 + j], ob);
-      }
-      const float2 dd = unpack2(add2(da, db)), oo = unpack2(add2(oa, ob));
-      float d = __fadd_rn(dd.x, dd.y), o = __fadd_rn(oo.x, oo.y);
-#pragma unroll
-      for (int off = LPR / 2; off >= 1; off >>= 1) {
-        d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, off));
-        o = __fadd_rn(o, __shfl_xor_sync(0xffffffffu, o, off));
-      }
-      const float vi = (FULL || rows[g] < p.V) ? v_s[t * VT + rows[g] - tile * VT] : 0.f;
-      const float u = __fmul_rn(be, __fsub_rn(vi, d));
-      o = __fmaf_rn(u, kq, o);
-      // S = H + u khat^T
-      const f32x2 u2 = pack2(u, u);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s[g][j] = fma2(u2, kk[j], s[g][j]);
-
-      if (FULL || rows[g] < p.V) {
-        if (writer) {
-          *optr[g] = o;
-          if (!NATIVE) *uptr[g] = u;
-        }
-        if (NATIVE) {
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            store_state_pairs(sptr[g] + 4 * LPR * m, s[g][2 * m], s[g][2 * m + 1]);
-        }
-      }
-      optr[g] += p.out_stride;
-      if (!NATIVE) uptr[g] += p.V;
-      if (NATIVE) sptr[g] += snap_step;
-    }
+  // ---- the tiles one after another, each loaded once its predecessor is done
+#pragma unroll 1
+  for (int i = 0; i < NS; ++i) {
+    if (i > 0) load_tile<K, ST, FULL>(s, S0, tile0 + i, p.V, warp, l, lr);
+    run_tile<K, ST, NATIVE, FULL>(s, p, tile0 + i, h, r, w, t0, i * VT, SV, kh_s, qh_s, v_s, al_s,
+                                  be_s, kq_s, warp, l, lr);
   }
 }
 
+template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS>
+static void launch_tiles(const VerifyParams& p, int ntiles, cudaStream_t stream) {
+  using Tile = VerifyTile<K>;
+  dim3 grid(ntiles / NS, p.HV, p.batch);
+  const size_t smem = sizeof(float) * verify_smem_floats<K>(p.W, NS);
+  gdn_verify_kernel<K, QKV, ST, NATIVE, FULL, NS><<<grid, Tile::THREADS, smem, stream>>>(p);
+}
+
+// The verify runs 4 (else 2) tiles of a head per CTA when they divide the
+// head; the native baseline, and heads smaller than a tile, one per CTA.
 template <int K, typename QKV, typename ST, bool NATIVE>
 static int launch_one(const VerifyParams& p, cudaStream_t stream) {
   using Tile = VerifyTile<K>;
   const int ntiles = (p.V + Tile::VT - 1) / Tile::VT;
-  dim3 grid(ntiles, p.HV, p.batch);
-  const size_t smem = sizeof(float) * verify_smem_floats<K>(p.W);
-  if (p.V % Tile::VT == 0)
-    gdn_verify_kernel<K, QKV, ST, NATIVE, true><<<grid, Tile::THREADS, smem, stream>>>(p);
-  else
-    gdn_verify_kernel<K, QKV, ST, NATIVE, false><<<grid, Tile::THREADS, smem, stream>>>(p);
+  const bool full = p.V % Tile::VT == 0;
+  bool done = false;
+  if constexpr (!NATIVE) {
+    if (full && ntiles % 4 == 0) {
+      launch_tiles<K, QKV, ST, NATIVE, true, 4>(p, ntiles, stream);
+      done = true;
+    } else if (full && ntiles % 2 == 0) {
+      launch_tiles<K, QKV, ST, NATIVE, true, 2>(p, ntiles, stream);
+      done = true;
+    }
+  }
+  if (!done) {
+    if (full) launch_tiles<K, QKV, ST, NATIVE, true, 1>(p, ntiles, stream);
+    else launch_tiles<K, QKV, ST, NATIVE, false, 1>(p, ntiles, stream);
+  }
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -286,10 +340,10 @@ int launch_verify(const VerifyParams& p, int head_k, int qkv_dtype, int state_dt
 
 size_t verify_smem_bytes(int head_k, int W) {
   switch (head_k) {
-    case 16: return sizeof(float) * verify_smem_floats<16>(W);
-    case 32: return sizeof(float) * verify_smem_floats<32>(W);
-    case 64: return sizeof(float) * verify_smem_floats<64>(W);
-    case 128: return sizeof(float) * verify_smem_floats<128>(W);
+    case 16: return sizeof(float) * verify_smem_floats<16>(W, 4);
+    case 32: return sizeof(float) * verify_smem_floats<32>(W, 4);
+    case 64: return sizeof(float) * verify_smem_floats<64>(W, 4);
+    case 128: return sizeof(float) * verify_smem_floats<128>(W, 4);
     default: return 0;
   }
 }
