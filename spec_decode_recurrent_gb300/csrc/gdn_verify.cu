@@ -31,6 +31,8 @@
 // every token instead, one tile per CTA.  Both run the identical per-token
 // arithmetic on every row, so their outputs agree bit for bit however the
 // tiles are grouped into CTAs, and the state update is the commit's fold.
+#include <type_traits>
+
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
 
@@ -98,8 +100,11 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
                      : nullptr;
   }
   const size_t snap_step = (size_t)p.HV * p.V * K;
-  // ---- the draft window, token by token, state in registers
-  for (int t = 0; t < w; ++t) {
+  // ---- the draft window, token by token, state in registers.  In VERIFY
+  // ---- mode the state after the last token is never read: that token runs
+  // ---- without the update.
+  auto token = [&](int t, auto update_tag) {
+    constexpr bool UPDATE = decltype(update_tag)::value;
     const float be = be_s[t], kq = kq_s[t];
     const f32x2 al2 = pack2(al_s[t], al_s[t]);
     f32x2 kk[8], qq[8];
@@ -137,9 +142,11 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
       const float u = __fmul_rn(be, __fsub_rn(vi, d));
       o = __fmaf_rn(u, kq, o);
       // S = H + u khat^T
-      const f32x2 u2 = pack2(u, u);
+      if (UPDATE) {
+        const f32x2 u2 = pack2(u, u);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s[g][j] = fma2(u2, kk[j], s[g][j]);
+        for (int j = 0; j < 8; ++j) s[g][j] = fma2(u2, kk[j], s[g][j]);
+      }
       if (FULL || rows[g] < p.V) {
         if (writer) {
           *optr[g] = o;
@@ -155,6 +162,12 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
       if (!NATIVE) uptr[g] += p.V;
       if (NATIVE) sptr[g] += snap_step;
     }
+  };
+  if constexpr (NATIVE) {
+    for (int t = 0; t < w; ++t) token(t, std::true_type{});
+  } else {
+    for (int t = 0; t + 1 < w; ++t) token(t, std::true_type{});
+    token(w - 1, std::false_type{});
   }
 }
 
