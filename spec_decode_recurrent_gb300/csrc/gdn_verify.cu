@@ -24,6 +24,9 @@
 // d = H khat and H qhat; then u = beta * (v - d), S = H + u khat^T and
 // o = S qhat evaluated as H qhat + u * (khat . qhat), the same value in
 // exact arithmetic with the output off the state update's critical path.
+// The two lane sums share their shuffles: one exchange leaves d on the lower
+// half of a row's lanes and o on the upper half, each half then sums its own
+// value, and d is broadcast back (4 shuffles per row and token, not 6).
 //
 // VERIFY mode writes o_t and the replay record (u_t, khat_t, alpha_t) and no
 // state (vLLM PR "[Spec Decode][Qwen4Exp] RecoverSSM for Qwen GDN and the
@@ -52,7 +55,7 @@ struct VerifyTile {
 // Dynamic shared memory of one verify CTA covering NS tiles, in floats.
 template <int K>
 __host__ __device__ constexpr int verify_smem_floats(int W, int NS) {
-  return W * (2 * K + NS * VerifyTile<K>::VT + 3);
+  return W * (2 * K + NS * VerifyTile<K>::VT + 4);
 }
 
 // Checkpoint rows of one tile into a register buffer (zeros past V).
@@ -80,12 +83,15 @@ template <int K, typename ST, bool NATIVE, bool FULL>
 __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], const VerifyParams& p,
                                          int tile, int h, int r, int w, long long t0, int vt_off,
                                          int vrow_stride, const float* kh_s, const float* qh_s,
-                                         const float* v_s, const float* al_s, const float* be_s,
-                                         const float* kq_s, int warp, int l, int lr) {
+                                         const float* v_s, const float* gs_s, int warp, int l, int lr) {
   using Tile = VerifyTile<K>;
   constexpr int LPR = Tile::LPR, RPW = Tile::RPW, RPT = Tile::RPT, VT = Tile::VT;
   const size_t rec_base = ((size_t)r * p.HV + h) * p.W;
-  const bool writer = (l == 0);
+  // the d half (lower LPR/2 lanes) and the o half of a row's lanes after
+  // the first exchange; the first o lane writes the row's outputs
+  const bool upper = LPR > 1 && (l & (LPR / 2)) != 0;
+  const int lane = lr * LPR + l;
+  const bool writer = (l == LPR / 2);
   int rows[RPT];
   float* optr[RPT];
   float* uptr[RPT];
@@ -105,8 +111,10 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
   // ---- without the update.
   auto token = [&](int t, auto update_tag) {
     constexpr bool UPDATE = decltype(update_tag)::value;
-    const float be = be_s[t], kq = kq_s[t];
-    const f32x2 al2 = pack2(al_s[t], al_s[t]);
+    const ulonglong2 gq = *reinterpret_cast<const ulonglong2*>(gs_s + 4 * t);
+    const f32x2 al2 = gq.x;  // (alpha, alpha)
+    const float2 bk = unpack2(gq.y);
+    const float be = bk.x, kq = bk.y;
     f32x2 kk[8], qq[8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -133,10 +141,15 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
       }
       const float2 dd = unpack2(add2(da, db)), oo = unpack2(add2(oa, ob));
       float d = __fadd_rn(dd.x, dd.y), o = __fadd_rn(oo.x, oo.y);
+      if (LPR > 1) {
+        // halving exchange: the d half keeps d and sends o, the o half the
+        // reverse; then each half sums its own value over its lanes
+        const float keep = upper ? o : d, send = upper ? d : o;
+        float x = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, LPR / 2));
 #pragma unroll
-      for (int off = LPR / 2; off >= 1; off >>= 1) {
-        d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, off));
-        o = __fadd_rn(o, __shfl_xor_sync(0xffffffffu, o, off));
+        for (int off = LPR / 4; off >= 1; off >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
+        d = __shfl_sync(0xffffffffu, x, lane - l);  // every lane takes d from the row's first lane
+        o = x;                                      // meaningful on the o half
       }
       const float vi = (FULL || rows[g] < p.V) ? v_s[t * vrow_stride + vt_off + rows[g] - tile * VT] : 0.f;
       const float u = __fmul_rn(be, __fsub_rn(vi, d));
@@ -218,9 +231,7 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS, VerifyTile<K>::MIN_CTA
   float* kh_s = smem;                   // [W][K]
   float* qh_s = kh_s + p.W * K;         // [W][K]
   float* v_s = qh_s + p.W * K;          // [W][SV]
-  float* al_s = v_s + p.W * SV;         // [W]
-  float* be_s = al_s + p.W;             // [W]
-  float* kq_s = be_s + p.W;             // [W]
+  float* gs_s = v_s + p.W * SV;         // [W][4]: alpha, alpha, beta, khat . qhat
   const QKV* qb = static_cast<const QKV*>(p.q);
   const QKV* kb = static_cast<const QKV*>(p.k);
   const QKV* vb = static_cast<const QKV*>(p.v);
@@ -260,13 +271,15 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS, VerifyTile<K>::MIN_CTA
       *reinterpret_cast<float4*>(kh_s + t * K + 4 * lane) = make_float4(kn[0], kn[1], kn[2], kn[3]);
       *reinterpret_cast<float4*>(qh_s + t * K + 4 * lane) = make_float4(qn[0], qn[1], qn[2], qn[3]);
     }
-    if (lane == 0) kq_s[t] = kq;
+    if (lane == 0) gs_s[4 * t + 3] = kq;
   }
   // gates of the whole window: one lane per token in the last warp
   if (warp == Tile::WARPS - 1 && lane < w) {
     const size_t gi = (size_t)(t0 + lane) * p.HV + h;
-    al_s[lane] = gate_decay(p.a[gi], p.A_log[h], p.dt_bias[h]);
-    be_s[lane] = gate_beta(p.b[gi]);
+    const float al = gate_decay(p.a[gi], p.A_log[h], p.dt_bias[h]);
+    gs_s[4 * lane] = al;
+    gs_s[4 * lane + 1] = al;
+    gs_s[4 * lane + 2] = gate_beta(p.b[gi]);
   }
   // the value rows of this CTA's tiles, every token, all threads
   for (int i = tid; i < w * SV; i += Tile::THREADS) {
@@ -278,15 +291,15 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS, VerifyTile<K>::MIN_CTA
   const size_t rec_base = ((size_t)r * p.HV + h) * p.W;  // record position 0
   if (!NATIVE && span == 0) {
     for (int i = tid; i < w * K; i += Tile::THREADS) p.rec_k[rec_base * K + i] = kh_s[i];
-    if (tid < w) p.rec_g[rec_base + tid] = al_s[tid];
+    if (tid < w) p.rec_g[rec_base + tid] = gs_s[4 * tid];
   }
 
   // ---- the tiles one after another, each loaded once its predecessor is done
 #pragma unroll 1
   for (int i = 0; i < NS; ++i) {
     if (i > 0) load_tile<K, ST, FULL>(s, S0, tile0 + i, p.V, warp, l, lr);
-    run_tile<K, ST, NATIVE, FULL>(s, p, tile0 + i, h, r, w, t0, i * VT, SV, kh_s, qh_s, v_s, al_s,
-                                  be_s, kq_s, warp, l, lr);
+    run_tile<K, ST, NATIVE, FULL>(s, p, tile0 + i, h, r, w, t0, i * VT, SV, kh_s, qh_s, v_s, gs_s,
+                                  warp, l, lr);
   }
 }
 
