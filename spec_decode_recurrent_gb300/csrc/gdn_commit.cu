@@ -21,9 +21,16 @@
 // therefore never read after it has been overwritten, which is the
 // guarantee "final folds before boundary folds" gives in a split commit.
 //
-// One CTA per (layer, row, head, 64-row tile): the record of the accepted
-// tokens is staged with per-thread asynchronous copies (cp.async) issued
-// ahead of the tile's loads, so four CTAs per SM keep ~128 KiB in flight.
+// fp32 states: one CTA per (layer, row, head, 64-row tile): the record of
+// the accepted tokens is staged with per-thread asynchronous copies
+// (cp.async) issued ahead of the tile's loads, so four CTAs per SM keep
+// ~128 KiB in flight.  bf16 states (gdn_commit_staged_kernel): one CTA per
+// whole head, the tile itself copied into shared memory with the record and
+// folded four chunks at a time, so four CTAs per SM again keep 128 KiB in
+// flight (a register-held bf16 tile would keep only half of that).
+//
+// Ordering: in both kernels every chunk of the tile is read before any of
+// it is written.
 #include "gdn_async.cuh"
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
@@ -204,6 +211,85 @@ __global__ void __launch_bounds__(kCommitThreads)
   store_chunks<ST, M, NT>(pool + ((size_t)plan.fin * p.HV + h) * head, x, c0, nchunks);
 }
 
+// bf16 states: a tile's widened fp32 values take twice the registers of its
+// bytes, which caps the bytes a register-held tile keeps in flight.  Here the
+// whole tile (a 128-row head) is first copied into shared memory by
+// asynchronous copies, together with the record, and then folded G chunks
+// at a time in registers; each element sees the same operations in the same
+// order as in gdn_commit_kernel, and every chunk is read before any chunk of
+// the tile is written, so a boundary or final slot equal to the source is
+// still safe.
+template <int K, typename ST, int M, int G>
+__global__ void __launch_bounds__(kCommitThreads)
+    gdn_commit_staged_kernel(const CommitParams p, int tiles_log2) {
+  using C = Chunk<ST>;
+  constexpr int E = C::E;
+  constexpr int CPR = K / E;
+  constexpr int NT = kCommitThreads;
+  constexpr int TILE_ROWS = NT * M / CPR;
+  extern __shared__ __align__(16) float smem[];
+
+  const int tile = blockIdx.x & ((1 << tiles_log2) - 1);
+  const int h = blockIdx.x >> tiles_log2;
+  const int r = blockIdx.y, layer = blockIdx.z;
+  const int tid = threadIdx.x;
+
+  const int32_t* trow = group_table_row(p, layer, r);
+  const RowCommit plan = commit_row_plan(p, r, trow);
+  if (plan.err) {
+    if (p.err && tid == 0 && tile == 0 && h == 0) atomicOr(p.err, plan.err);
+    return;
+  }
+  if (!plan.live) return;
+  const int n = plan.n;
+  const int row_base = tile * TILE_ROWS;
+  const int rows = min(TILE_ROWS, p.V - row_base);
+  if (rows <= 0) return;
+
+  float* u_s = smem;                     // [W][TILE_ROWS]
+  float* k_s = u_s + p.W * TILE_ROWS;    // [W][K]
+  float* g_s = k_s + p.W * K;            // [W]
+  ST* tile_s = reinterpret_cast<ST*>(g_s + ((p.W + 3) & ~3));  // [rows][K], 16-byte aligned
+  const size_t rec = ((size_t)r * p.HV + h) * p.W;
+  const float* ru = p.rec_u[layer] + rec * p.V + row_base;
+  const float* rk = p.rec_k[layer] + rec * K;
+  const float* rg = p.rec_g[layer] + rec;
+  const int urow4 = rows / 4;
+  for (int i = tid; i < n * urow4; i += NT)
+    cp_async16(u_s + (i / urow4) * TILE_ROWS + 4 * (i % urow4), ru + (size_t)(i / urow4) * p.V + 4 * (i % urow4));
+  for (int i = tid; i < n * (K / 4); i += NT) cp_async16(k_s + 4 * i, rk + 4 * i);
+  if (tid < n) cp_async4(g_s + tid, rg + tid);
+  const size_t head = (size_t)p.V * K;
+  ST* pool = static_cast<ST*>(p.pools[layer]);
+  const ST* S0 = pool + ((size_t)plan.src * p.HV + h) * head + (size_t)row_base * K;
+  for (int c = tid; c < rows * CPR; c += NT) cp_async16(tile_s + (size_t)c * E, S0 + (size_t)c * E);
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
+
+  const int nchunks = (row_base + rows) * CPR;  // end of this tile's chunks in the head
+  const int col = (tid % CPR) * E;
+#pragma unroll 1
+  for (int grp = 0; grp < M / G; ++grp) {
+    const int cg = row_base * CPR + tid + NT * G * grp;  // first chunk of this group (head index)
+    f32x2 x[G][E / 2];
+#pragma unroll
+    for (int m = 0; m < G; ++m) {
+      const int c = cg + NT * m;
+      if (c < nchunks) C::load_shared(tile_s + (size_t)(c - row_base * CPR) * E, x[m]);
+    }
+    for (int t = 0; t < n; ++t) {
+      fold_token<K, ST, G, NT>(x, g_s[t], k_s, u_s, t, TILE_ROWS, col, cg, row_base, nchunks);
+      const long long pos = plan.p0 + t + 1;
+      if (p.block_size > 0 && t + 1 < n && pos % p.block_size == 0) {
+        const int bs = slot_after(trow, p.table_stride, p.block_size, pos);
+        store_chunks<ST, G, NT>(pool + ((size_t)bs * p.HV + h) * head, x, cg, nchunks);
+      }
+    }
+    store_chunks<ST, G, NT>(pool + ((size_t)plan.fin * p.HV + h) * head, x, cg, nchunks);
+  }
+}
+
 // --------------------------------------------------------------- launchers
 template <int K, typename ST, int M>
 static int launch_commit_tiled_k(const CommitParams& p, cudaStream_t stream) {
@@ -232,13 +318,35 @@ static int launch_commit_k(const CommitParams& p, cudaStream_t stream) {
   return launch_commit_tiled_k<K, ST, M>(p, stream);
 }
 
+// bf16 states: whole 128-row heads staged in shared memory (see above).
+template <int K>
+static int launch_commit_bf16_k(const CommitParams& p, cudaStream_t stream) {
+  using ST = __nv_bfloat16;
+  constexpr int CPR = K / Chunk<ST>::E;
+  constexpr int M = (128 * CPR) / kCommitThreads > 0 ? (128 * CPR) / kCommitThreads : 1;
+  constexpr int G = M < 4 ? M : 4;
+  constexpr int TILE_ROWS = kCommitThreads * M / CPR;
+  const int tiles = (p.V + TILE_ROWS - 1) / TILE_ROWS;
+  int tiles_log2 = 0;
+  while ((1 << tiles_log2) < tiles) ++tiles_log2;
+  dim3 grid((unsigned)(p.HV << tiles_log2), p.batch, p.num_layers);
+  const size_t smem = sizeof(float) * ((size_t)p.W * (TILE_ROWS + K) + ((p.W + 3) & ~3)) +
+                      (size_t)TILE_ROWS * K * sizeof(ST);
+  auto kern = gdn_commit_staged_kernel<K, ST, M, G>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  kern<<<grid, kCommitThreads, smem, stream>>>(p, tiles_log2);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 int launch_commit(const CommitParams& p, int head_k, int state_dtype, cudaStream_t stream) {
   const bool bf = state_dtype == GDN_DTYPE_BF16;
   switch (head_k) {
-    case 16: return bf ? launch_commit_k<16, __nv_bfloat16>(p, stream) : launch_commit_k<16, float>(p, stream);
-    case 32: return bf ? launch_commit_k<32, __nv_bfloat16>(p, stream) : launch_commit_k<32, float>(p, stream);
-    case 64: return bf ? launch_commit_k<64, __nv_bfloat16>(p, stream) : launch_commit_k<64, float>(p, stream);
-    case 128: return bf ? launch_commit_k<128, __nv_bfloat16>(p, stream) : launch_commit_k<128, float>(p, stream);
+    case 16: return bf ? launch_commit_bf16_k<16>(p, stream) : launch_commit_k<16, float>(p, stream);
+    case 32: return bf ? launch_commit_bf16_k<32>(p, stream) : launch_commit_k<32, float>(p, stream);
+    case 64: return bf ? launch_commit_bf16_k<64>(p, stream) : launch_commit_k<64, float>(p, stream);
+    case 128: return bf ? launch_commit_bf16_k<128>(p, stream) : launch_commit_k<128, float>(p, stream);
     default: return GDN_ERR_UNSUPPORTED;
   }
 }
