@@ -77,6 +77,20 @@ SMALL = {
                                  accepted=[16, 13, 9, 12], block_size=4, seq_pos=[5, 8, 3, 1]),
     "align_block3_w6": dict(HK=1, HV=2, K=64, V=64, W=6, L=2, windows=[6, 6, 6, 3],
                             accepted=[6, 5, 3, 3], block_size=3, seq_pos=[1, 2, 3, 7]),
+    # two 32-row tiles per verify CTA (K = 128, V = 64), fp32 and bf16 state
+    "two_tile_span": dict(HK=1, HV=2, K=128, V=64, W=5, L=2, windows=[5, 2, 1, 5],
+                          accepted=[3, 2, 1, 5], qkv_dtype=wl.BF16),
+    "two_tile_span_bf16_state": dict(HK=1, HV=2, K=128, V=64, W=4, L=1, windows=[4, 3, 4],
+                                     accepted=[2, 3, 4], qkv_dtype=wl.BF16, state_dtype=wl.BF16),
+    # bf16 states at narrow heads: the shared-memory-staged commit with a
+    # tile taller than the head (ragged) and with two row tiles
+    "k64_bf16_state": dict(HK=2, HV=4, K=64, V=64, W=4, L=2, windows=[4, 1, 4],
+                           accepted=[4, 1, 3], state_dtype=wl.BF16),
+    "k32_v128_bf16_state": dict(HK=1, HV=2, K=32, V=128, W=3, L=1, windows=[3, 2],
+                                accepted=[1, 2], state_dtype=wl.BF16),
+    "k16_bf16_state_align": dict(HK=1, HV=1, K=16, V=32, W=6, L=1, windows=[6, 6],
+                                 accepted=[6, 4], block_size=2, seq_pos=[2, 5],
+                                 state_dtype=wl.BF16),
 }
 
 
