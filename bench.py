@@ -278,6 +278,11 @@ def run_gpu(args, rank, local_rank, world_size):
 
     commit_us = statistics.mean(commit_ms) * 1e3
     verify_us_layer = statistics.mean(verify_ms) * 1e3 / sb.L
+
+    def spread(ms, per=1):
+        """p10 / median / p90 of per-step event durations, in µs per launch."""
+        q = statistics.quantiles([x * 1e3 / per for x in ms], n=10) if len(ms) > 1 else [ms[0] * 1e3 / per] * 9
+        return {"p10": round(q[0], 2), "p50": round(statistics.median(ms) * 1e3 / per, 2), "p90": round(q[8], 2)}
     peak, peak_kind = measured_peaks()
     achieved = cbytes / (commit_us * 1e-6) / 1e9
     v_achieved = vbytes / (verify_us_layer * 1e-6) / 1e9
@@ -291,6 +296,7 @@ def run_gpu(args, rank, local_rank, world_size):
         "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
         "traffic": profiled_traffic("commit", args.workload, COMMIT_SOURCES),
         "algorithmic_bytes_per_launch": cbytes, "launch_us": round(commit_us, 2),
+        "launch_us_spread": spread(commit_ms),
         "share_of_step": round(commit_us / step_us, 4),
     }
     verify_rf = {
@@ -299,6 +305,7 @@ def run_gpu(args, rank, local_rank, world_size):
         "frac": round(v_achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
         "traffic": profiled_traffic("verify", args.workload, VERIFY_SOURCES),
         "algorithmic_bytes_per_launch": vbytes, "launch_us": round(verify_us_layer, 2),
+        "launch_us_spread": spread(verify_ms, sb.L),
         "share_of_step": round(verify_us_layer * sb.L / step_us, 4),
     }
     dominant, other = ((verify_rf, commit_rf) if verify_rf["share_of_step"] >= 0.5
