@@ -281,7 +281,7 @@ def run_gpu(args, rank, local_rank, world_size):
 
     def spread(ms, per=1):
         """p10 / median / p90 of per-step event durations, in µs per launch."""
-        q = statistics.quantiles([x * 1e3 / per for x in ms], n=10) if len(ms) > 1 else [ms[0] * 1e3 / per] * 9
+        q = statistics.quantiles([x * 1e3 / per for x in ms], n=10, method="inclusive") if len(ms) > 1 else [ms[0] * 1e3 / per] * 9
         return {"p10": round(q[0], 2), "p50": round(statistics.median(ms) * 1e3 / per, 2), "p90": round(q[8], 2)}
     peak, peak_kind = measured_peaks()
     achieved = cbytes / (commit_us * 1e-6) / 1e9
