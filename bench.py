@@ -198,11 +198,12 @@ VERIFY_SOURCES = ["spec_decode_recurrent_gb300/csrc/gdn_verify.cu",
                   "spec_decode_recurrent_gb300/csrc/gdn_device.cuh"]
 
 
-def profiled_traffic(kernel, workload, sources):
+def profiled_traffic(kernel, workload, sources, state_dtype="f32"):
     """DRAM bytes per launch from the committed ncu summary
-    profiles/<kernel>_<workload>.md, if it was taken from the current kernel
-    source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    profiles/<kernel>_<workload>[_bf16].md (the suffix for a bf16 state), if
+    it was taken from the current kernel source (else None)."""
+    suffix = "_bf16" if state_dtype == "bf16" else ""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}{suffix}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -294,7 +295,9 @@ def run_gpu(args, rank, local_rank, world_size):
         "kernel": "gdn_commit_kernel (all-layer replay commit, 1 launch per step)",
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-        "traffic": profiled_traffic("commit", args.workload, COMMIT_SOURCES),
+        # the summary covers the default layer count; a commit launch's bytes scale with it
+        "traffic": (profiled_traffic("commit", args.workload, COMMIT_SOURCES, args.state_dtype)
+                    if args.layers is None else None),
         "algorithmic_bytes_per_launch": cbytes, "launch_us": round(commit_us, 2),
         "launch_us_spread": spread(commit_ms),
         "share_of_step": round(commit_us / step_us, 4),
@@ -303,7 +306,7 @@ def run_gpu(args, rank, local_rank, world_size):
         "kernel": f"gdn_verify_kernel (verify of one layer, {sb.L} launches per step)",
         "bound": "hbm", "achieved": round(v_achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(v_achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-        "traffic": profiled_traffic("verify", args.workload, VERIFY_SOURCES),
+        "traffic": profiled_traffic("verify", args.workload, VERIFY_SOURCES, args.state_dtype),
         "algorithmic_bytes_per_launch": vbytes, "launch_us": round(verify_us_layer, 2),
         "launch_us_spread": spread(verify_ms, sb.L),
         "share_of_step": round(verify_us_layer * sb.L / step_us, 4),
