@@ -184,10 +184,16 @@ def measured_peaks():
 
 
 def source_hash(files):
+    """Hash of the kernel sources with comments and whitespace runs removed:
+    an edit to a comment leaves a profile's counters valid, a code edit
+    does not."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -304,9 +304,9 @@ static int launch_commit_tiled_k(const CommitParams& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-// A tile is 64 state rows (8 chunks per thread for a 128-wide fp32 state,
-// 4 for bf16): four such CTAs fit on an SM, and measured against whole-head
-// and 32-row tiles, and against a persistent kernel streaming heads through
+// fp32 states: a tile is 64 state rows (8 chunks per thread for a 128-wide
+// head): four such CTAs fit on an SM, and measured against whole-head and
+// 32-row tiles, and against a persistent kernel streaming heads through
 // shared memory with bulk asynchronous copies, it moves the most bytes.
 template <int K, typename ST>
 static int launch_commit_k(const CommitParams& p, cudaStream_t stream) {
