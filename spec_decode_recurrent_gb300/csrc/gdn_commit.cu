@@ -351,8 +351,4 @@ int launch_commit(const CommitParams& p, int head_k, int state_dtype, cudaStream
   }
 }
 
-size_t commit_smem_bytes(int head_k, int head_v, int W) {
-  return sizeof(float) * (size_t)W * (head_v + head_k + 1);
-}
-
 }  // namespace gdn

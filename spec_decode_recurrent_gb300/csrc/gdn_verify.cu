@@ -364,24 +364,4 @@ int launch_verify(const VerifyParams& p, int head_k, int qkv_dtype, int state_dt
   }
 }
 
-size_t verify_smem_bytes(int head_k, int W) {
-  switch (head_k) {
-    case 16: return sizeof(float) * verify_smem_floats<16>(W, 4);
-    case 32: return sizeof(float) * verify_smem_floats<32>(W, 4);
-    case 64: return sizeof(float) * verify_smem_floats<64>(W, 4);
-    case 128: return sizeof(float) * verify_smem_floats<128>(W, 4);
-    default: return 0;
-  }
-}
-
-int verify_rows_per_cta(int head_k) {
-  switch (head_k) {
-    case 16: return VerifyTile<16>::VT;
-    case 32: return VerifyTile<32>::VT;
-    case 64: return VerifyTile<64>::VT;
-    case 128: return VerifyTile<128>::VT;
-    default: return 0;
-  }
-}
-
 }  // namespace gdn
