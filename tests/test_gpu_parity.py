@@ -88,6 +88,10 @@ SMALL = {
                            accepted=[4, 1, 3], state_dtype=wl.BF16),
     "k32_v128_bf16_state": dict(HK=1, HV=2, K=32, V=128, W=3, L=1, windows=[3, 2],
                                 accepted=[1, 2], state_dtype=wl.BF16),
+    # window 16 with a bf16 state: the staged commit needs more than 48 KiB of
+    # shared memory per CTA (the opt-in path)
+    "max_window16_bf16_state": dict(HK=1, HV=2, K=128, V=128, W=16, L=1, windows=[16, 11],
+                                    accepted=[16, 5], qkv_dtype=wl.BF16, state_dtype=wl.BF16),
     "k16_bf16_state_align": dict(HK=1, HV=1, K=16, V=32, W=6, L=1, windows=[6, 6],
                                  accepted=[6, 4], block_size=2, seq_pos=[2, 5],
                                  state_dtype=wl.BF16),
