@@ -33,7 +33,9 @@
 // PLE short conv", Purpose).  NATIVE mode writes o_t and the full state after
 // every token instead, one tile per CTA.  Both run the identical per-token
 // arithmetic on every row, so their outputs agree bit for bit however the
-// tiles are grouped into CTAs, and the state update is the commit's fold.
+// tiles are grouped into CTAs, and the state update is the commit's fold
+// (which VERIFY mode skips after the window's last token: that state is
+// never read).
 #include <type_traits>
 
 #include "gdn_device.cuh"
