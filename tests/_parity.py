@@ -1,7 +1,6 @@
 """Helpers for the GPU parity tests: run the CUDA path through the C ABI on
 a SpecBatch, build the expected pools from the GPU native snapshots (for the
 bit-exact checks) and run the fp64 oracle (for the tolerance checks)."""
-import math
 import random
 
 import numpy as np

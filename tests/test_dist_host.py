@@ -3,7 +3,6 @@ barrier and the max-over-ranks timing reduction bench.py uses."""
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 
