@@ -36,6 +36,7 @@ from spec_decode_recurrent_gb300 import api, build, dist, roofline, step, worklo
 
 METRIC = "GDN verify+all-layer commit µs/step and achieved HBM GB/s vs ~8 TB/s roofline"
 UNIT = "us/step"
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth, reported beside the measured peak
 
 DESCR = {
     "all_layer": "36 GDN layers, batch 64 (56 live rows + 8 graph-padding rows with null slot "
@@ -301,6 +302,7 @@ def run_gpu(args, rank, local_rank, world_size):
         "kernel": "gdn_commit_kernel (all-layer replay commit, 1 launch per step)",
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+        "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
         # the summary covers the default layer count; a commit launch's bytes scale with it
         "traffic": (profiled_traffic("commit", args.workload, COMMIT_SOURCES, args.state_dtype)
                     if args.layers is None else None),
@@ -312,6 +314,7 @@ def run_gpu(args, rank, local_rank, world_size):
         "kernel": f"gdn_verify_kernel (verify of one layer, {sb.L} launches per step)",
         "bound": "hbm", "achieved": round(v_achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(v_achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+        "frac_of_nominal": round(v_achieved / NOMINAL_HBM_GBS, 4),
         "traffic": profiled_traffic("verify", args.workload, VERIFY_SOURCES, args.state_dtype),
         "algorithmic_bytes_per_launch": vbytes, "launch_us": round(verify_us_layer, 2),
         "launch_us_spread": spread(verify_ms, sb.L),
