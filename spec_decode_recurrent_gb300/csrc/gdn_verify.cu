@@ -8,9 +8,9 @@
 // gates and values are staged once per CTA for all of its tiles: that
 // staging and the row plan cost as many instructions as the recurrence of
 // one tile, so a head run as four separate tile CTAs paid them four times.
-// The tile buffer stays single (80 registers, six CTAs per SM): the CTAs of
-// one SM hide each other's tile loads better than a second register or
-// shared-memory buffer would.  Rows of S are independent given (khat, qhat,
+// The tile buffer stays single (80 registers and six CTAs per SM for an
+// fp32 state, 72 and seven for bf16): the CTAs of one SM hide each other's
+// tile loads better than a second register or shared-memory buffer would.  Rows of S are independent given (khat, qhat,
 // alpha, beta, v_i), so tiles never communicate; the only reductions are
 // over K, inside a group of K/16 lanes, by warp shuffles.
 //
@@ -51,11 +51,13 @@ struct VerifyTile {
   static constexpr int WARPS = 4;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int VT = WARPS * RPW * RPT;    // state rows per tile
-  // CTAs per SM the registers must allow: six for the verify (80 registers,
-  // no spills; measured faster than seven at 72 registers with spills), seven
-  // for the native form (72 registers, no spills).
-  static constexpr int MIN_CTAS_VERIFY = 6;
-  static constexpr int MIN_CTAS_NATIVE = 7;
+  // CTAs per SM the registers must allow, as measured: seven (72 registers)
+  // for the native form and for the verify with a bf16 state; six (80
+  // registers) for the verify with an fp32 state, which spills at 72.
+  template <bool NATIVE, typename ST>
+  static constexpr int min_ctas() {
+    return (!NATIVE && sizeof(ST) == 4) ? 6 : 7;
+  }
 };
 
 // Dynamic shared memory of one verify CTA covering NS tiles, in floats.
@@ -195,7 +197,7 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
 // then each tile's checkpoint rows are loaded and its window run in turn.
 template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS>
 __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
-                                  NATIVE ? VerifyTile<K>::MIN_CTAS_NATIVE : VerifyTile<K>::MIN_CTAS_VERIFY)
+                                  VerifyTile<K>::template min_ctas<NATIVE, ST>())
     gdn_verify_kernel(const VerifyParams p) {
   using Tile = VerifyTile<K>;
   constexpr int LPR = Tile::LPR, RPT = Tile::RPT, VT = Tile::VT;
