@@ -37,9 +37,14 @@
  *     failed launch).  Nothing is launched when the return is negative.
  *     batch == 0 launches nothing and checks only the shape (the per-row
  *     arrays of an empty batch may be NULL).
- *   - Row-level problems are found on the device: the row is skipped (it
- *     writes nothing) and its GDN_ROW_ERR_* bits are OR-ed into *err when
- *     err is not NULL.  The caller clears *err beforehand.
+ *   - Row-level problems are found on the device: the row is skipped and
+ *     its GDN_ROW_ERR_* bits are OR-ed into *err when err is not NULL.  The
+ *     caller clears *err beforehand.  A skipped row writes nothing, with one
+ *     exception: gdn_spec_verify marks a row it rejects by writing -1.0 (a
+ *     value no decay takes) into rec_g[r][h][0] for every head h, and
+ *     gdn_replay_commit stores nothing for a row whose record carries that
+ *     marker (GDN_ROW_ERR_REJECTED), so a verify-rejected row is never
+ *     committed even when no host code reads *err in between.
  *   - Null rows: a row whose window_len is 0 or whose checkpoint slot is -1
  *     reads and writes nothing (graph padding rows; vLLM PR above, Purpose).
  *   - Slot of the state after x folded tokens of row r:
@@ -83,6 +88,8 @@ extern "C" {
 #define GDN_ROW_ERR_TOKENS 32    /* token rows outside [0, num_tokens)                */
 #define GDN_ROW_ERR_GROUP 64     /* grouped commit: a layer's group id is outside     */
                                  /* [0, num_groups); that layer writes nothing       */
+#define GDN_ROW_ERR_REJECTED 128 /* commit: the verify rejected this row (its gate    */
+                                 /* record holds the reject marker); nothing stored  */
 
 typedef struct gdn_shape {
   int32_t num_k_heads; /* HK                                              */
@@ -155,7 +162,15 @@ int gdn_spec_verify(const gdn_shape* shape, int32_t batch, int32_t num_tokens,
  * checkpoint, so a boundary slot equal to the checkpoint slot is safe
  * (final folds before boundary folds).  A bf16 state is rounded once per
  * stored state (round to nearest even).  Rows with n == 0 or a null slot
- * write nothing.
+ * write nothing; a row whose gate record holds the verify's reject marker
+ * writes nothing and sets GDN_ROW_ERR_REJECTED.
+ *
+ * Slots are not shared between rows: every slot a live row writes (its final
+ * and boundary slots) must be neither read nor written by any other live
+ * row of the same call, in any layer group.  Rows run concurrently with no
+ * ordering between them, so a shared slot gives a timing-dependent result.
+ * Within one row, a boundary or final slot equal to its own checkpoint slot
+ * is fine (see above).
  */
 int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers,
                       int32_t batch, int32_t num_slots,
@@ -197,8 +212,9 @@ int gdn_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers,
 
 /*
  * Short-conv state commit over all layers in one launch (vLLM PR above,
- * Purpose: the short conv compacts its accepted window with the same plan;
- * Commits item 1: the commit's plan, conv and state steps).  A layer's
+ * Purpose: the short-conv state is advanced over the accepted tokens by the
+ * recurrent commit's own plan; Commits item 1: the commit's plan, conv and
+ * state steps).  A layer's
  * causal depthwise convolution of width state_len + 1 keeps, per slot and
  * channel, the last state_len convolution inputs, oldest first.  For each
  * live row with n = accepted_len[r] > 0 the state after x tokens -- the last

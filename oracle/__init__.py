@@ -85,6 +85,8 @@ def _load():
                 [_i] * 7 + [_D] * 3 + [_I, _I, _I, _I, _i, ctypes.c_long, _I, _i, _I, _i, _I])
             lib.gdn_oracle_num_threads.restype = _i
             lib.gdn_oracle_num_threads.argtypes = []
+            lib.gdn_oracle_set_num_threads.restype = None
+            lib.gdn_oracle_set_num_threads.argtypes = [_i]
             _lib = lib
     return _lib
 
@@ -113,6 +115,11 @@ def _ip(a):
 def num_threads() -> int:
     """OpenMP threads the oracle's parallel loops use."""
     return int(_load().gdn_oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on."""
+    _load().gdn_oracle_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- scalars

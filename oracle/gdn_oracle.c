@@ -60,6 +60,16 @@ int gdn_oracle_num_threads(void) {
 #endif
 }
 
+/* Threads the parallel loops use from now on (the benchmark times the
+ * oracle on all host cores and on one). */
+void gdn_oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* softplus(x) = log(1 + e^x), written so that neither branch overflows. */
 double gdn_oracle_softplus(double x) {
   if (x > 0.0) return x + log1p(exp(-x));
@@ -401,8 +411,8 @@ int gdn_oracle_replay_commit(int L, int HV, int K, int V, int W_max, int B,
       seq_pos, block_size, row_err);
 }
 
-/* Short-conv state commit (vLLM PR above, Purpose: the short conv "compacts
- * its accepted window with the same plan").  A layer's causal depthwise
+/* Short-conv state commit (vLLM PR above, Purpose: the conv state advances
+ * over the accepted tokens by the recurrent commit's plan).  A layer's causal depthwise
  * convolution of width SL + 1 keeps, per slot and channel, the last SL
  * convolution inputs, oldest first: state [C][SL].  The state after x
  * folded tokens of a row is the last SL entries of

@@ -20,7 +20,7 @@ from . import build as _build
 GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
 ROW_ERR_WINDOW, ROW_ERR_ACCEPTED, ROW_ERR_SLOT = 1, 2, 4
 ROW_ERR_BLOCK, ROW_ERR_SEQPOS, ROW_ERR_TOKENS = 8, 16, 32
-ROW_ERR_GROUP = 64
+ROW_ERR_GROUP, ROW_ERR_REJECTED = 64, 128
 ENTRY_POINTS = ("gdn_spec_verify", "gdn_replay_commit", "gdn_replay_commit_grouped",
                 "gdn_conv_state_commit", "gdn_native_spec_snapshot")
 

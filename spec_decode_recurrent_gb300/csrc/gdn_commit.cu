@@ -31,6 +31,12 @@
 //
 // Ordering: in both kernels every chunk of the tile is read before any of
 // it is written.
+//
+// Rows the verify rejected (token rows out of range, or any other row
+// error) carry the reject marker in gate record position 0; both kernels
+// check it once the record is staged and store nothing for such a row, so
+// a caller that replays verify and commit from one CUDA graph needs no host
+// round trip to keep a stale record out of the state.
 #include "gdn_async.cuh"
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
@@ -197,6 +203,10 @@ __global__ void __launch_bounds__(kCommitThreads)
   }
   cp_async_wait_all();
   __syncthreads();
+  if (g_s[0] < 0.f) {  // the verify rejected this row: nothing is stored
+    if (p.err && tid == 0 && tile == 0 && h == 0) atomicOr(p.err, GDN_ROW_ERR_REJECTED);
+    return;
+  }
 
   const int col = (tid % CPR) * E;  // fixed column block of this thread
   for (int t = 0; t < n; ++t) {
@@ -266,6 +276,10 @@ __global__ void __launch_bounds__(kCommitThreads)
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
+  if (g_s[0] < 0.f) {  // the verify rejected this row: nothing is stored
+    if (p.err && tid == 0 && tile == 0 && h == 0) atomicOr(p.err, GDN_ROW_ERR_REJECTED);
+    return;
+  }
 
   const int nchunks = (row_base + rows) * CPR;  // end of this tile's chunks in the head
   const int col = (tid % CPR) * E;

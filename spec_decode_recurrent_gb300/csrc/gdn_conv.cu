@@ -4,9 +4,9 @@
 // slot and channel, the last SL convolution inputs (oldest first).  After
 // sampling, that state must advance by the accepted tokens exactly as the
 // recurrent state does, with the same plan (vLLM PR "[Spec Decode][Qwen4Exp]
-// RecoverSSM for Qwen GDN and the PLE short conv", Purpose: the short conv
-// "compacts its accepted window with the same plan"; Commits item 1: plan,
-// conv and state steps of the commit).  The state after x folded tokens is
+// RecoverSSM for Qwen GDN and the PLE short conv", Purpose: the conv state
+// is advanced over the accepted tokens by the recurrent commit's plan;
+// Commits item 1: plan, conv and state steps of the commit).  The state after x folded tokens is
 // the last SL entries of (checkpoint state ++ the row's first x inputs),
 // written to the final slot and, in align mode, to every boundary slot.
 //

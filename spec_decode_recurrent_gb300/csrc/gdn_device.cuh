@@ -22,6 +22,10 @@ namespace gdn {
 
 constexpr int kMaxWindow = 16;
 constexpr float kL2NormEps = 1e-6f;
+// Written by the verify into gate record position 0 of every head of a row
+// it rejects; no decay exp(g) is negative, so the commit recognises it and
+// skips the row without storing anything.
+constexpr float kRejectedGate = -1.0f;
 
 // ------------------------------------------------------------ parameters
 struct VerifyParams {

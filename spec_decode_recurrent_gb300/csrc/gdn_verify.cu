@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   }
   if (src.err) {
     if (p.err && tid == 0 && span == 0 && h == 0) atomicOr(p.err, src.err);
+    // the reject marker tells the commit not to fold this row's stale record
+    if (!NATIVE && tid == 0 && span == 0) p.rec_g[((size_t)r * p.HV + h) * p.W] = kRejectedGate;
     return;
   }
   if (src.slot < 0) return;  // null row or empty window: writes nothing

@@ -61,12 +61,14 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("state_len", [3, 1, 8])
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("name", sorted(CASES))
+# every small case at every dtype and state length; the full-width case only
+# in the serving configuration (bf16 states, width-4 convolution)
+PARAMS = [(n, d, sl) for n in sorted(CASES) if n != "full_width_4_layers"
+          for d in ("bf16", "f32") for sl in (3, 1, 8)] + [("full_width_4_layers", "bf16", 3)]
+
+
+@pytest.mark.parametrize("name,dtype,state_len", PARAMS)
 def test_conv_commit_bit_exact(name, dtype, state_len):
-    if name == "full_width_4_layers" and (state_len != 3 or dtype != "bf16"):
-        pytest.skip("full width runs the serving configuration only")
     sb = CASES[name]()
     dt = wl.BF16 if dtype == "bf16" else wl.F32
     pools, inputs = wl.conv_state(sb, state_len=state_len, dtype=dt)

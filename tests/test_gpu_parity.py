@@ -5,8 +5,10 @@ against the GPU native per-draft-snapshot kernel.
   and committed state within tolerance, and untouched entries untouched;
 * full-size workloads in the launch configuration the benchmark times:
   verify == native and commit == native snapshot n bit for bit over every
-  layer, row and head (plus no stray pool writes), and sampled (layer, row,
-  head) units recomputed by the oracle.
+  layer, row and head (plus no stray pool writes), every native snapshot
+  written exactly inside the live windows, and sampled (layer, row, head)
+  units -- outputs, record, all snapshots and committed states --
+  recomputed by the oracle.
 """
 import gc
 
@@ -15,7 +17,7 @@ import pytest
 import torch
 
 from spec_decode_recurrent_gb300 import api, build, step, workloads as wl
-from tests._parity import GpuStep, compare_full, oracle_full
+from tests._parity import GpuStep, bits, compare_full, oracle_full
 
 pytestmark = pytest.mark.gpu
 
@@ -126,10 +128,10 @@ FULL = {
 def test_full_size_workload(name):
     sb = FULL[name]()
     try:
-        gs = GpuStep(sb)
+        gs = GpuStep(sb, units=12, unit_seed=len(name))
         assert gs.err == 0 and gs.verify_err == 0
         gs.check_bitwise()
-        for l, r, h in gs.units(12, seed=len(name)):
+        for l, r, h in gs.unit_list:
             gs.check_unit_against_oracle(l, r, h)
     finally:
         del sb
@@ -186,15 +188,36 @@ def test_malformed_rows_are_flagged_and_skipped():
     sb.accepted_len[1] = 3
     sb.slot_table[2, 0] = sb.num_slots + 5
     sb.window_len[3] = 5
-    sb.token_start[4] = sb.T - 1
-    sb.accepted_len[4] = 0        # a caller commits nothing for a row its verify rejected
+    sb.token_start[4] = sb.T - 1   # the commit skips it by the verify's reject marker
     gs = GpuStep(sb, native=False)
     assert gs.verify_err == api.ROW_ERR_SLOT | api.ROW_ERR_WINDOW | api.ROW_ERR_TOKENS
     assert gs.err == (api.ROW_ERR_SLOT | api.ROW_ERR_WINDOW | api.ROW_ERR_TOKENS
-                      | api.ROW_ERR_ACCEPTED)
+                      | api.ROW_ERR_ACCEPTED | api.ROW_ERR_REJECTED)
     changed = (sb.pools[0].view(torch.int32) != gs.before[0].view(torch.int32))
     slots = changed.flatten(1).any(1).nonzero().flatten().tolist()
     assert slots == [int(sb.slot_table[0, 0])]
+
+
+@pytest.mark.parametrize("state_dtype", [wl.F32, wl.BF16])
+def test_commit_skips_rows_the_verify_rejected(state_dtype):
+    # Row 1's window runs past the token rows: the verify rejects it and
+    # leaves a stale (here NaN-filled) record.  The caller commits without
+    # looking at the error word in between, with accepted_len > 0 for every
+    # row; row 1's slot must stay bitwise unchanged in every layer while the
+    # other rows commit as usual.
+    sb = wl.custom(device="cuda", HK=1, HV=2, K=128, V=128, W=4, L=2, windows=[4, 3, 4],
+                   accepted=[2, 3, 4], qkv_dtype=wl.BF16, state_dtype=state_dtype)
+    sb.token_start[1] = sb.T - 2
+    gs = GpuStep(sb, native=False)
+    assert gs.verify_err == api.ROW_ERR_TOKENS
+    assert gs.err == api.ROW_ERR_TOKENS | api.ROW_ERR_REJECTED
+    bad = int(sb.slot_table[1, 0])
+    for l in range(sb.L):
+        assert torch.equal(bits(sb.pools[l][bad]), bits(gs.before[l][bad])), f"layer {l}"
+        assert torch.equal(gs.bufs.rec_g[l][1, :, 0].cpu(), torch.full((sb.HV,), -1.0))
+        changed = (bits(sb.pools[l]) != bits(gs.before[l])).flatten(1).any(1)
+        assert changed.nonzero().flatten().tolist() == sorted(
+            int(sb.slot_table[r, 0]) for r in (0, 2))
 
 
 def test_align_missing_block_is_flagged():

@@ -33,6 +33,9 @@ MUTANTS = {
     "conv_window_off_by_one": ("for (int j = 0; j < SL; ++j) dst[j] = seq[ntok[w] + j];",
                                "for (int j = 0; j < SL; ++j) dst[j] = seq[ntok[w] + j - (j > 0)];"),
     "layer_group_ignored": ("int g = layer_group ? layer_group[l] : 0;", "int g = 0;"),
+    "boundary_fold_reads_written_pool": (
+        "memcpy(S, pools_in + l * pool_elems + ((size_t)src * HV + h) * VK,",
+        "memcpy(S, pools_out + l * pool_elems + ((size_t)src * HV + h) * VK,"),
     "source_one_token_late": (
         "int32_t s = slot_after(table_row, table_stride, block_size, seq_pos);",
         "int32_t s = slot_after(table_row, table_stride, block_size, seq_pos + 1);"),

@@ -291,6 +291,63 @@ def test_commit_equals_native_snapshot_states():
         assert np.allclose(pools[0], expect, rtol=1e-12, atol=1e-14)
 
 
+@pytest.mark.parametrize("Bk,W", [(4, 4), (3, 6), (2, 5)])
+def test_align_commit_writes_snapshots_into_boundary_and_final_slots(Bk, W):
+    # Align mode: the commit stores the state after p - p0 tokens into the
+    # slot of every block boundary p crossed, and the state after n tokens
+    # into the final slot.  Which slot gets which state comes from the
+    # token-by-token block walk (_brute_force_writes), the states from the
+    # oracle's own recompute (native snapshots): the commit replays records,
+    # so a wrong slot, a boundary off by one, a boundary fold that started
+    # from an already-written slot or a dropped final write all fail here.
+    # Rows cover every checkpoint offset p0 % Bk and every n in 1..W; when
+    # p0 % Bk != 0 and the window crosses a boundary, the boundary slot is
+    # the row's own checkpoint slot.
+    g = np.random.default_rng(7 + Bk)
+    HK, HV, K, V = 1, 2, 8, 8
+    combos = [(r, n) for r in range(Bk) for n in range(1, W + 1)]
+    B = len(combos)
+    seq_pos = np.array([Bk * (1 + i % 3) + r for i, (r, _) in enumerate(combos)], np.int32)
+    acc = np.array([n for _, n in combos], np.int32)
+    windows = np.full(B, W, np.int32)
+    stride = int((seq_pos.max() + W - 1) // Bk + 1)
+    table = np.full((B, stride), -1, np.int32)
+    nxt = 0
+    for r in range(B):
+        for col in range((seq_pos[r] - 1) // Bk, (seq_pos[r] + W - 1) // Bk + 1):
+            table[r, col] = nxt
+            nxt += 1
+    T = B * W
+    d = dict(q=g.normal(size=(T, HK, K)), k=g.normal(size=(T, HK, K)), v=g.normal(size=(T, HV, V)),
+             a=g.normal(size=(T, HV)), b=g.normal(size=(T, HV)), A_log=g.uniform(0, 2.7, HV),
+             dt_bias=g.uniform(-1, 1, HV), token_start=np.arange(0, T, W, dtype=np.int32),
+             window_len=windows, pool=g.normal(0, 0.1, (nxt, HV, V, K)), slot_table=table,
+             seq_pos=seq_pos, block_size=Bk, max_window=W)
+    v = oracle.spec_verify(**d, snapshots=True)
+    assert np.all(v["row_err"] == 0)
+    pools, err = oracle.replay_commit(
+        pools=d["pool"][None], rec_u=v["rec_u"][None], rec_k=v["rec_k"][None],
+        rec_g=v["rec_g"][None], window_len=windows, accepted_len=acc, slot_table=table,
+        seq_pos=seq_pos, block_size=Bk, max_window=W)
+    assert np.all(err == 0)
+    expect = d["pool"].copy()
+    src_reused = 0
+    for r in range(B):
+        p0, n = int(seq_pos[r]), int(acc[r])
+        cols = _brute_force_writes(p0, n, Bk)
+        for col, ntok in cols.items():
+            expect[table[r, col]] = v["snaps"][r, ntok - 1]
+        src_reused += int((p0 - 1) // Bk in cols)
+    assert src_reused > 0, "no row whose boundary slot is its checkpoint slot"
+    assert np.allclose(pools[0], expect, rtol=1e-12, atol=1e-14)
+    # slots no row writes keep the checkpoint bit for bit
+    written = {int(table[r, c]) for r in range(B)
+               for c in _brute_force_writes(int(seq_pos[r]), int(acc[r]), Bk)}
+    for s in range(nxt):
+        if s not in written:
+            assert np.array_equal(pools[0][s], d["pool"][s])
+
+
 def test_config_tiny_checkpoint_untouched_and_consistent():
     from spec_decode_recurrent_gb300 import workloads
     sb = workloads.tiny()
