@@ -11,8 +11,15 @@ conv-state commit) gets a write of twice the L2 size before every timed
 iteration, outside its events, so that each iteration starts cold; the
 36-layer steps touch ~100x the L2 and need none.
 
+The same run then measures every benchmark configuration (tiny, the
+one-layer serving shape, the three long/ragged seeds, align mode with fp32
+and bf16 states) and reports µs per verify, per native snapshot and per
+all-layer commit with their HBM fractions in the line's `configs` block.
+
 Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
-instead, on a bounded sample of the same workload.
+instead: whole steps of the same workload when they fit the time budget,
+else a bounded sample of each step.  --gpus N without a torchrun
+environment re-launches this script under torchrun with N ranks.
 """
 from __future__ import annotations
 
@@ -39,6 +46,8 @@ UNIT = "us/step"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth, reported beside the measured peak
 
 DESCR = {
+    "tiny": "1 GDN layer, batch 2, HK=HV=2, K=V=16, window 4, accepted [1,3], fp32 q/k/v and "
+            "state, slots [0,1], seed 0",
     "all_layer": "36 GDN layers, batch 64 (56 live rows + 8 graph-padding rows with null slot "
                  "and window 0), HK=16 HV=32 K=V=128, window 4 (MTP 3), accepted uniform 1..4, "
                  "bf16 q/k/v, fp32 [V,K] state, slots a random permutation of a 256-slot pool, seed 2",
@@ -53,7 +62,7 @@ DESCR = {
 }
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser(description=__doc__)
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=500)
@@ -71,15 +80,21 @@ def parse():
     p.add_argument("--grouped-commit", action="store_true",
                    help="measure the grouped commit (3 KV-cache groups x 6 layers, one launch) "
                         "against one commit call per group; prints its own JSON line")
-    return p.parse_args()
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the per-configuration block (profiler runs)")
+    p.add_argument("--seed", type=int, default=None, help="workload seed (default: its own)")
+    return p.parse_args(argv)
 
 
-def make_workload(name, device, rank, state_dtype, layers=None):
+DEFAULT_SEED = {"tiny": 0, "all_layer": 2, "layer": 1, "long_ragged": 30, "align": 4, "mtp5": 5}
+
+
+def make_workload(name, device, rank, state_dtype, layers=None, seed=None):
     fn = workloads.WORKLOADS[name]
     kw = dict(device=device, sentinel=False)
     if layers is not None:
         kw["L"] = layers
-    base = {"all_layer": 2, "layer": 1, "long_ragged": 30, "align": 4, "mtp5": 5}[name]
+    base = DEFAULT_SEED[name] if seed is None else seed
     kw["seed"] = dist.replica_seed(base, rank)
     if state_dtype == torch.bfloat16:
         import inspect
@@ -149,29 +164,50 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- peaks
+def l2_bytes(dev=None):
+    """L2 size of the device (GB300: ~126 MB); the nominal size without one."""
+    if torch.cuda.is_available():
+        return int(torch.cuda.get_device_properties(dev or 0).L2_cache_size)
+    return 126 * 1024 * 1024
+
+
+def l2_rule(footprint, l2):
+    """(flush?, description) for a timed unit touching `footprint` bytes."""
+    mb = footprint / 1e6
+    if footprint < 3 * l2:
+        return True, (f"flush: {mb:.0f} MB per timed unit < 3x the {l2 / 1e6:.0f} MB L2; before "
+                      f"every timed iteration, outside its events, a {2 * l2 / 1e6:.0f} MB buffer "
+                      f"is written and another {2 * l2 / 1e6:.0f} MB buffer read, so the unit "
+                      "starts with none of its data in L2 and no dirty lines left to write back")
+    return False, (f"no flush: inputs larger than L2 ({mb / 1e3:.1f} GB per step vs "
+                   f"{l2 / 1e9:.2f} GB L2)")
+
+
 class L2Scrub:
-    """Writes a buffer of twice the L2 size before a timed iteration when the
-    timed unit's bytes are under three times the L2 (else does nothing)."""
+    """Before a timed iteration whose bytes are under three times the L2:
+    write a buffer of twice the L2 size (evicting the unit's data), then read
+    another of twice the L2 size, so that the write's dirty lines drain to
+    DRAM here, outside the timed region, instead of during the timed kernel
+    (which would then pay for writing back a buffer it never touched)."""
 
     def __init__(self, dev, footprint):
-        self.l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+        self.l2 = l2_bytes(dev)
         self.footprint = int(footprint)
-        self.on = self.footprint < 3 * self.l2
-        self.buf = torch.empty(2 * self.l2 // 4, dtype=torch.float32, device=dev) if self.on else None
+        self.on, self.text = l2_rule(self.footprint, self.l2)
+        n = 2 * self.l2 // 4
+        self.wbuf = torch.empty(n, dtype=torch.float32, device=dev) if self.on else None
+        self.rbuf = torch.ones(n, dtype=torch.float32, device=dev) if self.on else None
+        self.sink = torch.empty((), dtype=torch.float32, device=dev) if self.on else None
         self.n = 0
 
     def __call__(self):
         if self.on:
             self.n += 1
-            self.buf.fill_(float(self.n & 1))
+            self.wbuf.fill_(float(self.n & 1))
+            torch.sum(self.rbuf, dim=0, out=self.sink)
 
     def describe(self):
-        mb = self.footprint / 1e6
-        if self.on:
-            return (f"flush: {mb:.0f} MB per timed unit < 3x the {self.l2 / 1e6:.0f} MB L2; a "
-                    f"{2 * self.l2 / 1e6:.0f} MB buffer is written before every timed iteration, "
-                    "outside its events")
-        return f"no flush: inputs larger than L2 ({mb / 1e3:.1f} GB per step vs {self.l2 / 1e9:.2f} GB L2)"
+        return self.text
 
 
 def measured_peaks():
@@ -221,6 +257,29 @@ def profiled_traffic(kernel, workload, sources, state_dtype="f32"):
     return float(t.group(1))
 
 
+def workload_text(args):
+    text = f"{args.workload}: {DESCR[args.workload]}"
+    if args.seed is not None:
+        text += f" (seed overridden: {args.seed})"
+    return text
+
+
+def config_dict(args, sb, world_size):
+    """The `config` object of the JSON line; both arms print the same one."""
+    footprint = roofline.commit_bytes(sb) + roofline.verify_bytes_per_layer(sb) * sb.L
+    return {
+        "workload": workload_text(args),
+        "layers": sb.L, "batch": sb.B, "heads_k": sb.HK, "heads_v": sb.HV,
+        "head_k": sb.K, "head_v": sb.V, "window": sb.W,
+        "state_dtype": args.state_dtype,
+        "qkv_dtype": "bf16" if sb.qkv_dtype == torch.bfloat16 else "f32",
+        "parallelism": f"replicas x{world_size} (no collective on the path)",
+        "l2": l2_rule(footprint, l2_bytes())[1],
+        "step": "verify of every layer (CUDA graph of the per-layer API calls) + one "
+                "all-layer commit call",
+    }
+
+
 # ---------------------------------------------------------- the GPU arm
 def run_gpu(args, rank, local_rank, world_size):
     torch.cuda.set_device(local_rank)
@@ -228,7 +287,7 @@ def run_gpu(args, rank, local_rank, world_size):
     build.build()
     api.load()
     sd = torch.bfloat16 if args.state_dtype == "bf16" else torch.float32
-    sb = make_workload(args.workload, dev, rank, sd, args.layers)
+    sb = make_workload(args.workload, dev, rank, sd, args.layers, args.seed)
     arena = step.pack_inputs(sb)   # one contiguous buffer of the step's inputs
     bufs = step.StepBuffers(sb)
     stream = torch.cuda.current_stream()
@@ -256,7 +315,7 @@ def run_gpu(args, rank, local_rank, world_size):
     cbytes = roofline.commit_bytes(sb)
     vbytes = roofline.verify_bytes_per_layer(sb)
     scrub = L2Scrub(dev, cbytes + vbytes * sb.L)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     clocks = ClockSampler(dev)
     clocks.start()
     time.sleep(0.3)
@@ -268,18 +327,20 @@ def run_gpu(args, rank, local_rank, world_size):
         ev[i][0].record(stream)
         graph.replay()
         ev[i][1].record(stream)
-        step.commit(sb, bufs)
+        scrub()     # a small step: the commit starts cold too, as after a model's forward
         ev[i][2].record(stream)
+        step.commit(sb, bufs)
+        ev[i][3].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     dist.barrier()
     clk = clocks.stop()
     # device time of the K steps: back to back without a scrub, the sum of
-    # the steps' own events with one (the scrub writes fall between them)
-    total_ms = (sum(e[0].elapsed_time(e[2]) for e in ev) if scrub.on
-                else ev[0][0].elapsed_time(ev[-1][2]))
+    # the verify and commit events with one (the scrubs fall between them)
     verify_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    commit_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    commit_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    total_ms = (sum(verify_ms) + sum(commit_ms) if scrub.on
+                else ev[0][0].elapsed_time(ev[-1][3]))
     assert int(bufs.err.item()) == 0, "row errors in the benchmark workload"
     total_ms = dist.max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / K
@@ -320,6 +381,15 @@ def run_gpu(args, rank, local_rank, world_size):
         "launch_us_spread": spread(verify_ms, sb.L),
         "share_of_step": round(verify_us_layer * sb.L / step_us, 4),
     }
+    for rf in (commit_rf, verify_rf):
+        # the DRAM bytes ncu counted for the same launch, over the same time
+        rf["achieved_dram_gbs"] = (round(rf["traffic"] / (rf["launch_us"] * 1e-6) / 1e9, 1)
+                                   if rf["traffic"] else None)
+        rf["note"] = ("achieved = algorithmic bytes / event time; frac can exceed 1 because the "
+                      "peak is a plain copy (torch copy_, 1:1 read:write) and because writes "
+                      "still dirty in L2 when the kernel ends drain after its end event "
+                      "(achieved_dram_gbs: the DRAM bytes ncu counted for one launch over the "
+                      "same time)")
     dominant, other = ((verify_rf, commit_rf) if verify_rf["share_of_step"] >= 0.5
                        else (commit_rf, verify_rf))
 
@@ -353,16 +423,7 @@ def run_gpu(args, rank, local_rank, world_size):
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; see workloads.py)",
-        "config": {
-            "workload": f"{args.workload}: {DESCR[args.workload]}",
-            "layers": sb.L, "batch": sb.B, "heads_k": sb.HK, "heads_v": sb.HV,
-            "head_k": sb.K, "head_v": sb.V, "window": sb.W,
-            "state_dtype": args.state_dtype, "qkv_dtype": "bf16" if sb.qkv_dtype == torch.bfloat16 else "f32",
-            "parallelism": f"replicas x{world_size} (no collective on the path)",
-            "l2": scrub.describe(),
-            "step": "verify of every layer (CUDA graph of the per-layer API calls) + one "
-                    "all-layer commit call",
-        },
+        "config": config_dict(args, sb, world_size),
         "roofline": dominant,
         "other_roofline": other,
         "native_snapshot": {
@@ -380,7 +441,127 @@ def run_gpu(args, rank, local_rank, world_size):
         result["e2e"] = e2e
     if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(sb, args.cpu_seconds)
+    if not args.no_configs and args.layers is None and args.seed is None:
+        main_entry = {
+            "workload": DESCR[args.workload], "layers": sb.L, "batch": sb.B, "window": sb.W,
+            "state_dtype": args.state_dtype, "step_us": round(step_us, 2),
+            "verify_us_per_layer": round(verify_us_layer, 2),
+            "verify_bytes_per_layer": vbytes, "verify_gbs": round(v_achieved, 1),
+            "verify_frac": round(v_achieved / peak, 4),
+            "native_us_per_layer": round(native_us, 2), "native_bytes_per_layer": nbytes,
+            "native_gbs": round(nbytes / (native_us * 1e-6) / 1e9, 1),
+            "commit_us": round(commit_us, 2), "commit_bytes": cbytes,
+            "commit_gbs": round(achieved, 1), "commit_frac": round(achieved / peak, 4),
+            "l2": scrub.describe(), "steps": K, "source": "the line's own timed steps"}
+        del sb, bufs, graph, arena
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        result["configs"] = run_configs(args, dev, rank, stream, peak,
+                                        {(args.workload, args.state_dtype): main_entry})
     return result
+
+
+# Every benchmark configuration, measured in the same run: (key, workload,
+# state dtype, seed).  The long/ragged configuration runs its three seeds.
+CONFIGS = [
+    ("tiny", "tiny", "f32", None),
+    ("layer", "layer", "f32", None),
+    ("all_layer", "all_layer", "f32", None),
+    ("long_ragged_seed30", "long_ragged", "f32", 30),
+    ("long_ragged_seed31", "long_ragged", "f32", 31),
+    ("long_ragged_seed32", "long_ragged", "f32", 32),
+    ("align_fp32", "align", "f32", None),
+    ("align_bf16", "align", "bf16", None),
+]
+
+
+def measure_config(sb, dev, stream, peak, steps, warmup=3):
+    """µs per verify (one layer), per native snapshot (one layer) and per
+    all-layer commit on one workload, with their algorithmic bytes and HBM
+    fractions.  The verify of all layers runs from a CUDA graph, the commit
+    eagerly, as in the main step; a workload under three times the L2 gets
+    the clean scrub before its verify and before its commit."""
+    bufs = step.StepBuffers(sb)
+    step.verify_all(sb, bufs)
+    step.commit(sb, bufs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.verify_all(sb, bufs)
+    torch.cuda.synchronize()
+    cbytes = roofline.commit_bytes(sb)
+    vbytes = roofline.verify_bytes_per_layer(sb)
+    scrub = L2Scrub(dev, cbytes + vbytes * sb.L)
+    for _ in range(warmup):
+        graph.replay()
+        step.commit(sb, bufs)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        scrub()
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+        scrub()
+        ev[i][2].record(stream)
+        step.commit(sb, bufs)
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0, "row errors in a benchmark workload"
+    verify_us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3 / sb.L
+    commit_us = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) * 1e3
+    del graph, bufs
+    out_n, snaps = step.native_buffers(sb)
+    step.native_layer(sb, 0, out_n, snaps)
+    torch.cuda.synchronize()
+    reps = max(sb.L, 8)
+    nbytes = roofline.native_bytes_per_layer(sb)
+    nscrub = L2Scrub(dev, nbytes * min(sb.L, reps))
+    nev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for i in range(reps):
+        nscrub()
+        nev[i][0].record(stream)
+        step.native_layer(sb, i % sb.L, out_n, snaps)
+        nev[i][1].record(stream)
+    torch.cuda.synchronize()
+    native_us = sum(a.elapsed_time(b) for a, b in nev) * 1e3 / reps
+    del out_n, snaps
+    gbs = lambda b, us: b / (us * 1e-6) / 1e9
+    return {
+        "layers": sb.L, "batch": sb.B, "window": sb.W,
+        "step_us": round(verify_us * sb.L + commit_us, 2),
+        "verify_us_per_layer": round(verify_us, 2), "verify_bytes_per_layer": vbytes,
+        "verify_gbs": round(gbs(vbytes, verify_us), 1),
+        "verify_frac": round(gbs(vbytes, verify_us) / peak, 4),
+        "native_us_per_layer": round(native_us, 2), "native_bytes_per_layer": nbytes,
+        "native_gbs": round(gbs(nbytes, native_us), 1),
+        "commit_us": round(commit_us, 2), "commit_bytes": cbytes,
+        "commit_gbs": round(gbs(cbytes, commit_us), 1),
+        "commit_frac": round(gbs(cbytes, commit_us) / peak, 4),
+        "l2": scrub.describe(), "steps": steps,
+    }
+
+
+def run_configs(args, dev, rank, stream, peak, done):
+    """The `configs` block: every configuration in CONFIGS, one workload in
+    memory at a time (the main workload's numbers are reused)."""
+    out = {}
+    steps = max(5, min(args.steps, 20))
+    for key, name, sdt, seed in CONFIGS:
+        if seed is None and (name, sdt) in done:
+            out[key] = done[(name, sdt)]
+            continue
+        sd = torch.bfloat16 if sdt == "bf16" else torch.float32
+        sb = make_workload(name, dev, rank, sd, seed=seed)
+        entry = {"workload": DESCR[name] if seed is None else
+                 re.sub(r"seed \d+", f"seed {seed}", DESCR[name]), "state_dtype": sdt}
+        entry.update(measure_config(sb, dev, stream, peak, steps))
+        out[key] = entry
+        del sb
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    out["peak"] = {"hbm_gbs": peak, "kind": "measured copy bandwidth"}
+    return out
 
 
 def run_conv_commit(sb, stream, peak, dev, state_len=3):
@@ -624,83 +805,137 @@ def _compact_layer(sb, l, rows):
                 dt_bias=f64(sb.dt_bias[l]), token_start=new_start.numpy(), window_len=win.numpy(),
                 pool=pool, slot_table=new_table.numpy(),
                 seq_pos=None if sb.seq_pos is None else sb.seq_pos[rows].cpu().numpy(),
-                accepted_len=sb.accepted_len[rows].cpu().numpy())
+                accepted_len=sb.accepted_len[rows].cpu().numpy(), block_size=sb.block_size,
+                W=sb.W)
 
 
-def _oracle_unit_of_work(oracle, d, sb):
+def _oracle_unit_of_work(oracle, d):
+    """Oracle verify, then commit, of one compacted layer."""
     v = oracle.spec_verify(q=d["q"], k=d["k"], v=d["v"], a=d["a"], b=d["b"], A_log=d["A_log"],
                            dt_bias=d["dt_bias"], token_start=d["token_start"],
                            window_len=d["window_len"], pool=d["pool"],
                            slot_table=d["slot_table"], seq_pos=d["seq_pos"],
-                           block_size=sb.block_size, max_window=sb.W)
+                           block_size=d["block_size"], max_window=d["W"])
     oracle.replay_commit(pools=d["pool"][None], rec_u=v["rec_u"][None], rec_k=v["rec_k"][None],
                          rec_g=v["rec_g"][None], window_len=d["window_len"],
                          accepted_len=d["accepted_len"], slot_table=d["slot_table"],
-                         seq_pos=d["seq_pos"], block_size=sb.block_size, max_window=sb.W)
+                         seq_pos=d["seq_pos"], block_size=d["block_size"], max_window=d["W"])
 
 
-def cpu_baseline(sb, seconds):
-    """The fp64 oracle as it stands, on the host cores, over whole layers of
-    the same workload until the time budget is spent; scaled to a full step."""
-    import oracle
-    oracle.build()
+def _time_layers(oracle, sb, seconds):
+    """Oracle verify + commit over whole layers (all rows) until `seconds` of
+    oracle time are spent; returns (layers done, seconds).  The host copies
+    each layer needs are made outside the timed calls."""
     rows = list(range(sb.B))
     layers_done, spent = 0, 0.0
     for l in range(sb.L):
         d = _compact_layer(sb, l, rows)
         t0 = time.perf_counter()
-        _oracle_unit_of_work(oracle, d, sb)
+        _oracle_unit_of_work(oracle, d)
         spent += time.perf_counter() - t0
         layers_done += 1
         if spent >= seconds:
             break
-    us = spent / layers_done * sb.L * 1e6
-    return {"value": round(us, 1), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{layers_done} of {sb.L} layers (all {sb.B} rows), verify + commit, "
-                      f"{spent:.1f} s of CPU wall time, scaled to {sb.L} layers"}
+    return layers_done, spent
+
+
+def cpu_baseline(sb, seconds, seconds_one_core=6.0):
+    """The fp64 oracle as it stands, on all host cores and on one, over whole
+    layers of the same workload until each time budget is spent; scaled to a
+    full step."""
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    n_all, t_all = _time_layers(oracle, sb, seconds)
+    oracle.set_num_threads(1)
+    try:
+        n_one, t_one = _time_layers(oracle, sb, seconds_one_core)
+    finally:
+        oracle.set_num_threads(cores)
+    scaled = lambda n, t: round(t / n * sb.L * 1e6, 1)
+    return {"value": scaled(n_all, t_all), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_all} of {sb.L} layers (all {sb.B} rows), verify + commit, "
+                      f"{t_all:.1f} s of oracle time on {cores} threads, scaled to {sb.L} layers",
+            "single_core": {"value": scaled(n_one, t_one), "unit": UNIT, "cores": 1,
+                            "sample": f"{n_one} of {sb.L} layers (all {sb.B} rows), "
+                                      f"{t_one:.1f} s of oracle time on 1 thread, scaled to "
+                                      f"{sb.L} layers"}}
 
 
 # ------------------------------------------------------ reference arm
+REFERENCE_BUDGET_S = 150.0
+
+
 def run_reference(args, rank, world_size):
-    """The oracle on this workload, timed on the host cores: every step is a
-    bounded sample (a few rows of one layer), scaled to the full step."""
+    """The oracle on this workload, timed on the host cores.  Each step runs
+    verify + commit of every layer over all rows when K + W such steps fit
+    the time budget; otherwise each step runs a cycling subset of the layers
+    (all rows), scaled to the full step.  Under torchrun only rank 0 works;
+    the other ranks join the process group and leave."""
+    if world_size > 1:
+        dist.init("gloo")
+    try:
+        if rank != 0:
+            dist.barrier()
+            return None
+        result = _reference_rank0(args, world_size)
+        dist.barrier()
+        return result
+    finally:
+        dist.finalize()
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _reference_rank0(args, world_size):
     import oracle
     oracle.build()
+    # all of the host's cores (torchrun would otherwise leave one thread per rank)
+    oracle.set_num_threads(host_cores())
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     sd = torch.bfloat16 if args.state_dtype == "bf16" else torch.float32
-    sb = make_workload(args.workload, dev, 0, sd)
-    live = [r for r in range(sb.B) if int(sb.window_len[r]) > 0 and int(sb.slot_table[r, 0]) >= 0] \
-        if sb.block_size == 0 else list(range(sb.B))
+    sb = make_workload(args.workload, dev, 0, sd, args.layers, args.seed)
+    rows = list(range(sb.B))
+    layers = [_compact_layer(sb, l, rows) for l in range(sb.L)]   # host copies, once
+    config = config_dict(args, sb, world_size)
+    del sb
+
+    def run_layers(ids):
+        for l in ids:
+            _oracle_unit_of_work(oracle, layers[l])
+
     n_steps = args.warmup + args.steps
-    budget = max(0.02, min(1.0, 150.0 / n_steps))
-    # size the per-step row sample against the budget
-    d1 = _compact_layer(sb, 0, live[:1])
     t0 = time.perf_counter()
-    _oracle_unit_of_work(oracle, d1, sb)
-    per_row = max(time.perf_counter() - t0, 1e-4)
-    nrows = max(1, min(len(live), int(budget / per_row)))
-    samples = []
+    run_layers([0])
+    per_layer = time.perf_counter() - t0
+    L = len(layers)
+    m = L if n_steps * per_layer * L <= REFERENCE_BUDGET_S else \
+        max(1, min(L, int(REFERENCE_BUDGET_S / (n_steps * per_layer))))
+    samples, nxt = [], 0
     for i in range(n_steps):
-        l = i % sb.L
-        rows = [live[(i * nrows + j) % len(live)] for j in range(nrows)]
-        d = _compact_layer(sb, l, rows)
+        ids = [(nxt + j) % L for j in range(m)]
+        nxt = (nxt + m) % L
         t0 = time.perf_counter()
-        _oracle_unit_of_work(oracle, d, sb)
+        run_layers(ids)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             samples.append(dt)
-    per_step = statistics.mean(samples) * (len(live) / nrows) * sb.L
-    us = per_step * 1e6
-    sample = (f"each step: {nrows} of {len(live)} live rows of one layer (verify + commit), "
-              f"scaled to {len(live)} rows x {sb.L} layers")
+    us = statistics.mean(samples) * (L / m) * 1e6
+    sample = (f"each step: verify + commit of all {L} layers x {len(rows)} rows (the whole step)"
+              if m == L else
+              f"each step: verify + commit of {m} of {L} layers (cycling) x all {len(rows)} rows, "
+              f"scaled to {L} layers to keep {n_steps} steps within {REFERENCE_BUDGET_S:.0f} s")
     return {
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
         "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; see workloads.py)",
-        "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
-                   "state_dtype": args.state_dtype},
+        "config": config,
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -708,13 +943,38 @@ def run_reference(args, rank, world_size):
     }
 
 
-def main():
-    args = parse()
+# ------------------------------------------------------------ launcher
+def _free_port():
+    import socket
+    s_ = socket.socket()
+    s_.bind(("127.0.0.1", 0))
+    port = s_.getsockname()[1]
+    s_.close()
+    return port
+
+
+def relaunch(argv, n):
+    """Run this script under torchrun with n ranks on this node (one per
+    GPU), passing the same arguments; returns torchrun's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1",
+           "--master-port", str(_free_port()), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
+    args = parse(argv)
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return relaunch(argv, args.gpus)
     rank, local_rank, world_size = dist.world()
+    if "WORLD_SIZE" in os.environ and world_size != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world_size}", file=sys.stderr)
+        return 2
     if args.impl == "reference":
-        if rank != 0:
-            return 0
-        print(json.dumps(run_reference(args, rank, world_size)), flush=True)
+        res = run_reference(args, rank, world_size)
+        if res is not None:
+            print(json.dumps(res), flush=True)
         return 0
     if args.grouped_commit:
         print(json.dumps(run_grouped(args)), flush=True)

@@ -90,6 +90,9 @@ extern "C" {
                                  /* [0, num_groups); that layer writes nothing       */
 #define GDN_ROW_ERR_REJECTED 128 /* commit: the verify rejected this row (its gate    */
                                  /* record holds the reject marker); nothing stored  */
+#define GDN_ROW_ERR_TIMEOUT 256  /* a CTA gave up waiting for its own asynchronous    */
+                                 /* copy (never expected); its remaining work is not */
+                                 /* done and the call's outputs are incomplete       */
 
 typedef struct gdn_shape {
   int32_t num_k_heads; /* HK                                              */

@@ -247,19 +247,32 @@ __device__ __forceinline__ int slot_after(const int32_t* row, int stride,
   return row[col];
 }
 
-__device__ __forceinline__ SourceSlot source_slot(int w, int W, const int32_t* row,
-                                                  int stride, int block_size,
-                                                  const int32_t* seq_pos, int r,
-                                                  int num_slots) {
+// The row's scalars a plan needs, requested together at the start of a
+// kernel (each is in bounds for any row r < batch), so the plan costs one
+// memory round trip instead of a chain of dependent ones.
+struct RowScalars {
+  int w;          // window_len[r]
+  int slot0;      // slot_table[r][0]
+  long long sp;   // seq_pos[r] (align mode), else 0
+};
+__device__ __forceinline__ RowScalars row_scalars(const int32_t* window_len, const int32_t* trow,
+                                                  const int32_t* seq_pos, int block_size, int r) {
+  RowScalars x;
+  x.w = window_len[r];
+  x.slot0 = trow[0];
+  x.sp = block_size > 0 ? seq_pos[r] : 0;
+  return x;
+}
+
+__device__ __forceinline__ SourceSlot source_slot(const RowScalars& x, int W, const int32_t* row,
+                                                  int stride, int block_size, int num_slots) {
   SourceSlot s{-1, 0};
+  const int w = x.w;
   if (w < 0 || w > W) { s.err = GDN_ROW_ERR_WINDOW; return s; }
   if (w == 0) return s;
-  long long p0 = 0;
-  if (block_size > 0) {
-    p0 = seq_pos[r];
-    if (p0 < 1) { s.err = GDN_ROW_ERR_SEQPOS; return s; }
-  }
-  int slot = slot_after(row, stride, block_size, p0);
+  const long long p0 = x.sp;
+  if (block_size > 0 && p0 < 1) { s.err = GDN_ROW_ERR_SEQPOS; return s; }
+  int slot = block_size == 0 ? x.slot0 : slot_after(row, stride, block_size, p0);
   if (slot == kOutsideTable) { s.err = GDN_ROW_ERR_BLOCK; return s; }
   if (slot < -1 || slot >= num_slots) { s.err = GDN_ROW_ERR_SLOT; return s; }
   s.slot = slot;
@@ -278,13 +291,24 @@ struct RowCommit {
   long long p0;  // tokens already in the checkpoint (align mode)
 };
 
+__device__ __forceinline__ RowScalars row_scalars_from(int w, const int32_t* trow,
+                                                       const int32_t* seq_pos, int block_size,
+                                                       int r) {
+  RowScalars x;
+  x.w = w;
+  x.slot0 = trow[0];
+  x.sp = block_size > 0 ? seq_pos[r] : 0;
+  return x;
+}
+
 __device__ __forceinline__ RowCommit row_commit_plan(int w, int n, const int32_t* trow,
                                                      int stride, int block_size,
                                                      const int32_t* seq_pos, int r,
                                                      int num_slots, int W) {
   RowCommit c{0, false, -1, -1, 0, 0};
   if (trow == nullptr) { c.err = GDN_ROW_ERR_GROUP; return c; }
-  SourceSlot src = source_slot(w, W, trow, stride, block_size, seq_pos, r, num_slots);
+  const RowScalars x = row_scalars_from(w, trow, seq_pos, block_size, r);
+  SourceSlot src = source_slot(x, W, trow, stride, block_size, num_slots);
   if (src.err) { c.err = src.err; return c; }
   if (n < 0 || n > w) { c.err = GDN_ROW_ERR_ACCEPTED; return c; }
   if (src.slot < 0 || n == 0) return c;

@@ -8,11 +8,15 @@
 // gates and values are staged once per CTA for all of its tiles: that
 // staging and the row plan cost as many instructions as the recurrence of
 // one tile, so a head run as four separate tile CTAs paid them four times.
-// The tile buffer stays single (80 registers and six CTAs per SM for an
-// fp32 state, 72 and seven for bf16): the CTAs of one SM hide each other's
-// tile loads better than a second register or shared-memory buffer would.  Rows of S are independent given (khat, qhat,
-// alpha, beta, v_i), so tiles never communicate; the only reductions are
-// over K, inside a group of K/16 lanes, by warp shuffles.
+// Tiles reach the CTA as single bulk copies (cp.async.bulk, one thread, one
+// instruction per 16 KiB tile) into one shared-memory buffer, completed
+// through an mbarrier: tile i + 1 is requested as soon as every warp has
+// moved tile i into registers, so it streams in while tile i runs (80
+// registers and six CTAs per SM for an fp32 state, 72 and seven for bf16).
+// A CTA with a single tile (the native form) loads it straight into
+// registers.  Rows of S are independent given (khat, qhat, alpha, beta,
+// v_i), so tiles never communicate; the only reductions are over K, inside
+// a group of K/16 lanes, by warp shuffles.
 //
 // Register layout of a tile, for K = 128: LPR = 8 lanes share one state row
 // and each lane holds 16 of its columns, as four 4-column chunks at columns
@@ -38,6 +42,7 @@
 // never read).
 #include <type_traits>
 
+#include "gdn_async.cuh"
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
 
@@ -60,10 +65,50 @@ struct VerifyTile {
   }
 };
 
-// Dynamic shared memory of one verify CTA covering NS tiles, in floats.
+// Dynamic shared memory of one verify CTA covering NS tiles, in bytes: the
+// mbarrier (16 bytes), the tile buffer the bulk copies fill (NS > 1 only),
+// then the staged keys, queries, values and gates.
+template <int K, typename ST>
+__host__ __device__ constexpr size_t verify_tile_bytes(int NS) {
+  return NS > 1 ? (size_t)VerifyTile<K>::VT * K * sizeof(ST) : 0;
+}
+template <int K, typename ST>
+__host__ __device__ constexpr size_t verify_smem_bytes(int W, int NS) {
+  return 16 + verify_tile_bytes<K, ST>(NS) +
+         sizeof(float) * (size_t)W * (2 * K + NS * VerifyTile<K>::VT + 4);
+}
+
+// A tile's checkpoint rows from the shared-memory tile buffer (a verbatim
+// copy of VT contiguous state rows) into the register buffer.
 template <int K>
-__host__ __device__ constexpr int verify_smem_floats(int W, int NS) {
-  return W * (2 * K + NS * VerifyTile<K>::VT + 4);
+__device__ __forceinline__ void load_tile_shared(f32x2 (&s)[VerifyTile<K>::RPT][8], const float* buf,
+                                                 int warp, int l, int lr) {
+  using Tile = VerifyTile<K>;
+#pragma unroll
+  for (int g = 0; g < Tile::RPT; ++g) {
+    const int row = (g * Tile::WARPS + warp) * Tile::RPW + lr;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const ulonglong2 t = *reinterpret_cast<const ulonglong2*>(buf + row * K + 4 * (l + Tile::LPR * m));
+      s[g][2 * m] = t.x;
+      s[g][2 * m + 1] = t.y;
+    }
+  }
+}
+template <int K>
+__device__ __forceinline__ void load_tile_shared(f32x2 (&s)[VerifyTile<K>::RPT][8],
+                                                 const __nv_bfloat16* buf, int warp, int l, int lr) {
+  using Tile = VerifyTile<K>;
+#pragma unroll
+  for (int g = 0; g < Tile::RPT; ++g) {
+    const int row = (g * Tile::WARPS + warp) * Tile::RPW + lr;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint2 t = *reinterpret_cast<const uint2*>(buf + row * K + 4 * (l + Tile::LPR * m));
+      s[g][2 * m] = pack2(bf16_bits_to_float(t.x & 0xffffu), bf16_bits_to_float(t.x >> 16));
+      s[g][2 * m + 1] = pack2(bf16_bits_to_float(t.y & 0xffffu), bf16_bits_to_float(t.y >> 16));
+    }
+  }
 }
 
 // Checkpoint rows of one tile into a register buffer (zeros past V).
@@ -201,20 +246,24 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
     gdn_verify_kernel(const VerifyParams p) {
   using Tile = VerifyTile<K>;
   constexpr int LPR = Tile::LPR, RPT = Tile::RPT, VT = Tile::VT;
-  extern __shared__ float smem[];
+  constexpr bool BULK = NS > 1;  // tiles arrive by bulk copies into shared memory
+  static_assert(!BULK || FULL, "bulk-copied tiles are whole tiles");
+  extern __shared__ __align__(16) unsigned char smem_raw[];
 
   const int span = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile0 = span * NS;  // first tile of this CTA
 
-  // ---- row plan: identical checks in every CTA of the row
-  const int w = p.window_len[r];
+  // ---- row plan: identical checks in every CTA of the row.  The row's
+  // ---- scalars are requested together, not one after another.
   const int32_t* trow = p.slot_table + (size_t)r * p.table_stride;
-  SourceSlot src = source_slot(w, p.W, trow, p.table_stride, p.block_size,
-                               p.seq_pos, r, p.num_slots);
+  const RowScalars rs = row_scalars(p.window_len, trow, p.seq_pos, p.block_size, r);
+  const long long t0_raw = p.token_start[r];
+  const int w = rs.w;
+  SourceSlot src = source_slot(rs, p.W, trow, p.table_stride, p.block_size, p.num_slots);
   long long t0 = 0;
   if (!src.err && src.slot >= 0) {
-    t0 = p.token_start[r];
+    t0 = t0_raw;
     if (t0 < 0 || t0 + w > p.num_tokens) src.err = GDN_ROW_ERR_TOKENS;
   }
   if (src.err) {
@@ -233,13 +282,25 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   // ---- while the window's inputs are staged.  Row group g holds columns
   // ---- 4*(l + LPR*m) + {0..3}: s[g][2m] = +0,+1 and s[g][2m+1] = +2,+3.
   const ST* S0 = static_cast<const ST*>(p.pool) + ((size_t)src.slot * p.HV + h) * (size_t)p.V * K;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
+  ST* tbuf = reinterpret_cast<ST*>(smem_raw + 16);
+  constexpr uint32_t kTileBytes = (uint32_t)verify_tile_bytes<K, ST>(NS);
   f32x2 s[RPT][8];
-  load_tile<K, ST, FULL>(s, S0, tile0, p.V, warp, l, lr);
+  if constexpr (BULK) {
+    // one thread requests the first tile as a single bulk copy
+    if (tid == 0) {
+      mbar_init(bar, 1);
+      mbar_expect_tx(bar, kTileBytes);
+      bulk_load(tbuf, S0 + (size_t)tile0 * VT * K, kTileBytes, bar);
+    }
+  } else {
+    load_tile<K, ST, FULL>(s, S0, tile0, p.V, warp, l, lr);
+  }
 
   // ---- stage normalised keys / queries, their dot product, the gates and
   // ---- the value rows of all NS tiles for the whole window in shared memory
   constexpr int SV = NS * VT;           // staged value rows
-  float* kh_s = smem;                   // [W][K]
+  float* kh_s = reinterpret_cast<float*>(smem_raw + 16 + kTileBytes);  // [W][K]
   float* qh_s = kh_s + p.W * K;         // [W][K]
   float* v_s = qh_s + p.W * K;          // [W][SV]
   float* gs_s = v_s + p.W * SV;         // [W][4]: alpha, alpha, beta, khat . qhat
@@ -305,10 +366,28 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
     if (tid < w) p.rec_g[rec_base + tid] = gs_s[4 * tid];
   }
 
-  // ---- the tiles one after another, each loaded once its predecessor is done
+  // ---- the tiles one after another.  With bulk copies, tile i + 1 is
+  // ---- requested into the (single) shared buffer as soon as every warp has
+  // ---- moved tile i into registers, so it streams in while tile i runs.
 #pragma unroll 1
   for (int i = 0; i < NS; ++i) {
-    if (i > 0) load_tile<K, ST, FULL>(s, S0, tile0 + i, p.V, warp, l, lr);
+    if constexpr (BULK) {
+      const bool ok = mbar_wait(bar, i & 1);
+      if (ok) load_tile_shared<K>(s, tbuf, warp, l, lr);
+      if (__syncthreads_or(!ok)) {
+        // never expected: report, let the copy in flight land, and stop
+        if (tid == 0 && p.err) atomicOr(p.err, GDN_ROW_ERR_TIMEOUT);
+        mbar_wait(bar, i & 1);
+        return;
+      }
+      if (tid == 0 && i + 1 < NS) {
+        fence_proxy_async_shared();
+        mbar_expect_tx(bar, kTileBytes);
+        bulk_load(tbuf, S0 + (size_t)(tile0 + i + 1) * VT * K, kTileBytes, bar);
+      }
+    } else {
+      if (i > 0) load_tile<K, ST, FULL>(s, S0, tile0 + i, p.V, warp, l, lr);
+    }
     run_tile<K, ST, NATIVE, FULL>(s, p, tile0 + i, h, r, w, t0, i * VT, SV, kh_s, qh_s, v_s, gs_s,
                                   warp, l, lr);
   }
@@ -318,8 +397,11 @@ template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS>
 static void launch_tiles(const VerifyParams& p, int ntiles, cudaStream_t stream) {
   using Tile = VerifyTile<K>;
   dim3 grid(ntiles / NS, p.HV, p.batch);
-  const size_t smem = sizeof(float) * verify_smem_floats<K>(p.W, NS);
-  gdn_verify_kernel<K, QKV, ST, NATIVE, FULL, NS><<<grid, Tile::THREADS, smem, stream>>>(p);
+  const size_t smem = verify_smem_bytes<K, ST>(p.W, NS);
+  auto kern = gdn_verify_kernel<K, QKV, ST, NATIVE, FULL, NS>;
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  kern<<<grid, Tile::THREADS, smem, stream>>>(p);
 }
 
 // The verify runs 4 (else 2) tiles of a head per CTA when they divide the
