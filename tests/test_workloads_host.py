@@ -73,9 +73,11 @@ def test_bench_cpu_baseline_helpers_run_on_cpu():
     import bench
     sb = wl.all_layer(L=2, batch=6, pad_rows=1, HK=2, HV=4, KV=16, num_slots=12, sentinel=False)
     d = bench._compact_layer(sb, 0, list(range(sb.B)))
-    bench._oracle_unit_of_work(oracle, d, sb)
-    res = bench.cpu_baseline(sb, 0.01)
+    bench._oracle_unit_of_work(oracle, d)
+    res = bench.cpu_baseline(sb, 0.01, 0.01)
     assert res["value"] > 0 and res["cores"] >= 1
+    assert res["single_core"]["cores"] == 1 and res["single_core"]["value"] > 0
+    assert oracle.num_threads() == res["cores"]      # the thread count is restored
 
 
 @pytest.mark.parametrize("fused", [False, True])
