@@ -83,6 +83,17 @@ def _load():
             lib.gdn_oracle_conv_commit.restype = _i
             lib.gdn_oracle_conv_commit.argtypes = (
                 [_i] * 7 + [_D] * 3 + [_I, _I, _I, _I, _i, ctypes.c_long, _I, _i, _I, _i, _I])
+            lib.gdn_oracle_kda_window.restype = None
+            lib.gdn_oracle_kda_window.argtypes = [_i, _i, _i, _D, _D, _D, _D, _D, _D,
+                                                  ctypes.c_double, _D, _D, _D, _D, _D, _D]
+            lib.gdn_oracle_kda_replay.restype = None
+            lib.gdn_oracle_kda_replay.argtypes = [_i, _i, _i, _D, _D, _D, _D]
+            lib.gdn_oracle_kda_spec_verify.restype = _i
+            lib.gdn_oracle_kda_spec_verify.argtypes = (
+                [_i] * 8 + [_D] * 7 + [_I, _I, _D, _I, _i, _I, _i] + [_D] * 5 + [_I])
+            lib.gdn_oracle_kda_replay_commit.restype = _i
+            lib.gdn_oracle_kda_replay_commit.argtypes = (
+                [_i] * 7 + [_D] * 5 + [_I, _I, _I, _i, _I, _i, _I])
             lib.gdn_oracle_num_threads.restype = _i
             lib.gdn_oracle_num_threads.argtypes = []
             lib.gdn_oracle_set_num_threads.restype = None
@@ -312,4 +323,86 @@ def conv_commit(*, pools, inputs, token_start, window_len, accepted_len, slot_ta
         int(block_size), _ip(row_err))
     if rc != 0:
         raise ValueError(f"oracle conv_commit rejected the shape ({rc})")
+    return pools_out, row_err
+
+
+# --------------------------------------------------- KDA (per-channel decay)
+def kda_window(S0, q, k, v, a, b, A_log: float, dt_bias):
+    """KDA verify window of one unit: a [w, K] per-channel gate inputs,
+    dt_bias [K]; otherwise as window().  alpha comes back as [w, K]."""
+    S0 = _f64(S0)
+    V, K = S0.shape
+    q, k, v, a, b, dt_bias = (_f64(t) for t in (q, k, v, a, b, dt_bias))
+    w = b.shape[0]
+    o = np.empty((w, V)); u = np.empty((w, V)); kh = np.empty((w, K))
+    al = np.empty((w, K)); st = np.empty((w, V, K))
+    _load().gdn_oracle_kda_window(K, V, w, _dp(S0), _dp(q), _dp(k), _dp(v), _dp(a), _dp(b),
+                                  float(A_log), _dp(dt_bias), _dp(o), _dp(u), _dp(kh),
+                                  _dp(al), _dp(st))
+    return {"o": o, "u": u, "khat": kh, "alpha": al, "states": st}
+
+
+def kda_replay(S0, u, khat, alpha) -> np.ndarray:
+    """Fold len(alpha) KDA records (alpha [n, K]) into a copy of S0 [V, K]."""
+    S = _f64(S0).copy()
+    V, K = S.shape
+    u, khat, alpha = _f64(u), _f64(khat), _f64(alpha).reshape(-1, K)
+    _load().gdn_oracle_kda_replay(K, V, alpha.shape[0], _dp(S), _dp(u), _dp(khat), _dp(alpha))
+    return S
+
+
+def kda_spec_verify(*, q, k, v, a, b, A_log, dt_bias, token_start, window_len, pool,
+                    slot_table, seq_pos=None, block_size=0, max_window, snapshots=False):
+    """KDA verify for one layer: a [T, HV, K], dt_bias [HV, K]; returns the
+    same dict as spec_verify with rec_g [B, HV, W, K]."""
+    q, k, v, a, b = (_f64(t) for t in (q, k, v, a, b))
+    A_log, dt_bias, pool = _f64(A_log), _f64(dt_bias), _f64(pool)
+    token_start, window_len = _i32(token_start), _i32(window_len)
+    slot_table = _i32(slot_table)
+    if slot_table.ndim == 1:
+        slot_table = slot_table.reshape(-1, 1)
+    T, HK, K = k.shape
+    HV, V = v.shape[1], v.shape[2]
+    B = window_len.shape[0]
+    W = int(max_window)
+    sp = None if seq_pos is None else _i32(seq_pos)
+    nan = np.nan
+    out = np.full((T, HV, V), nan)
+    rec_u = np.full((B, HV, W, V), nan)
+    rec_k = np.full((B, HV, W, K), nan)
+    rec_g = np.full((B, HV, W, K), nan)
+    snaps = np.full((B, W, HV, V, K), nan) if snapshots else None
+    row_err = np.zeros(B, dtype=np.int32)
+    rc = _load().gdn_oracle_kda_spec_verify(
+        HK, HV, K, V, W, B, T, pool.shape[0], _dp(q), _dp(k), _dp(v), _dp(a), _dp(b),
+        _dp(A_log), _dp(dt_bias), _ip(token_start), _ip(window_len), _dp(pool),
+        _ip(slot_table), slot_table.shape[1], _ip(sp), int(block_size),
+        _dp(out), _dp(rec_u), _dp(rec_k), _dp(rec_g), _dp(snaps), _ip(row_err))
+    if rc != 0:
+        raise ValueError(f"oracle kda_spec_verify rejected the shape ({rc})")
+    return {"out": out, "rec_u": rec_u, "rec_k": rec_k, "rec_g": rec_g, "snaps": snaps,
+            "row_err": row_err}
+
+
+def kda_replay_commit(*, pools, rec_u, rec_k, rec_g, window_len, accepted_len, slot_table,
+                      seq_pos=None, block_size=0, max_window):
+    """All-layer KDA commit from records: rec_g [L, B, HV, W, K].
+    Returns (new_pools float64, row_err)."""
+    pools_in = _f64(pools)
+    pools_out = pools_in.copy()
+    rec_u, rec_k, rec_g = _f64(rec_u), _f64(rec_k), _f64(rec_g)
+    window_len, accepted_len = _i32(window_len), _i32(accepted_len)
+    slot_table = _i32(slot_table)
+    if slot_table.ndim == 1:
+        slot_table = slot_table.reshape(-1, 1)
+    L, num_slots, HV, V, K = pools_in.shape
+    B = window_len.shape[0]
+    sp = None if seq_pos is None else _i32(seq_pos)
+    row_err = np.zeros(B, dtype=np.int32)
+    rc = _load().gdn_oracle_kda_replay_commit(
+        L, HV, K, V, int(max_window), B, num_slots, _dp(pools_in), _dp(pools_out),
+        _dp(rec_u), _dp(rec_k), _dp(rec_g), _ip(window_len), _ip(accepted_len),
+        _ip(slot_table), slot_table.shape[1], _ip(sp), int(block_size), _ip(row_err))
+    if rc != 0:
+        raise ValueError(f"oracle kda_replay_commit rejected the shape ({rc})")
     return pools_out, row_err

@@ -469,3 +469,217 @@ int gdn_oracle_conv_commit(int L, int C, int SL, int W_max, int B, int T,
   free(seq);
   return 0;
 }
+
+/* ------------------------------------------------------------------ KDA
+ * Per-channel decay (KDA, the Kimi Delta Attention layer the protocol was
+ * first built for: tokenspeed PR "feat: add Qwen3.5 GDN ReplaySSM",
+ * Summary; vLLM PR above, Purpose).  The pages print no KDA formula; the
+ * reading taken here replaces the scalar decay of the gated delta rule by a
+ * vector over the K key channels, everything else unchanged:
+ *   alpha_t[j] = exp(-exp(A_log) * softplus(a_t[j] + dt_bias[j])),  j < K
+ *   H          = S_{t-1} diag(alpha_t)   (column j of S scaled by alpha_t[j])
+ *   u_t        = beta_t * (v_t - H khat_t)
+ *   S_t        = H + u_t khat_t^T
+ *   o_t        = S_t qhat_t
+ * and the replay record keeps the whole gate vector: (u_t, khat_t, alpha_t
+ * in R^K).  The commit's fold is S = alpha_t-scaled columns plus the
+ * rank-one write, token by token. */
+
+/* One KDA token on S[V][K], in place; alpha[K] is the gate vector. */
+static void kda_token_step(int K, int V, double* S, const double* khat,
+                           const double* qhat, const double* v,
+                           const double* alpha, double beta, double* u_out,
+                           double* o_out) {
+  /* H = S diag(alpha): every element of column j scaled by alpha[j] */
+  for (int i = 0; i < V; ++i)
+    for (int j = 0; j < K; ++j) S[(size_t)i * K + j] *= alpha[j];
+  /* u = beta * (v - H khat) */
+  for (int i = 0; i < V; ++i) {
+    double d = 0.0;
+    for (int j = 0; j < K; ++j) d += S[(size_t)i * K + j] * khat[j];
+    u_out[i] = beta * (v[i] - d);
+  }
+  /* S = H + u khat^T */
+  for (int i = 0; i < V; ++i)
+    for (int j = 0; j < K; ++j) S[(size_t)i * K + j] += u_out[i] * khat[j];
+  /* o = S qhat */
+  for (int i = 0; i < V; ++i) {
+    double o = 0.0;
+    for (int j = 0; j < K; ++j) o += S[(size_t)i * K + j] * qhat[j];
+    o_out[i] = o;
+  }
+}
+
+/* The KDA verify window of one (request, value head) unit.
+ *   a [w][K] raw per-channel gate inputs, dt_bias [K]; otherwise as
+ *   gdn_oracle_window.  alpha (optional) receives [w][K] gate vectors. */
+void gdn_oracle_kda_window(int K, int V, int w, const double* S0,
+                           const double* q, const double* k, const double* v,
+                           const double* a, const double* b, double A_log,
+                           const double* dt_bias, double* o, double* u,
+                           double* khat, double* alpha, double* states) {
+  size_t VK = (size_t)V * K;
+  double* S = (double*)malloc(VK * sizeof(double));
+  double* kh = (double*)malloc((size_t)K * sizeof(double));
+  double* qh = (double*)malloc((size_t)K * sizeof(double));
+  double* al = (double*)malloc((size_t)K * sizeof(double));
+  double* ut = (double*)malloc((size_t)V * sizeof(double));
+  double* ot = (double*)malloc((size_t)V * sizeof(double));
+  memcpy(S, S0, VK * sizeof(double));
+  for (int t = 0; t < w; ++t) {
+    for (int j = 0; j < K; ++j)
+      al[j] = gdn_oracle_decay(a[(size_t)t * K + j], A_log, dt_bias[j]);
+    double be = gdn_oracle_beta(b[t]);
+    gdn_oracle_l2norm(K, k + (size_t)t * K, kh);
+    gdn_oracle_l2norm(K, q + (size_t)t * K, qh);
+    kda_token_step(K, V, S, kh, qh, v + (size_t)t * V, al, be, ut, ot);
+    if (o) memcpy(o + (size_t)t * V, ot, (size_t)V * sizeof(double));
+    if (u) memcpy(u + (size_t)t * V, ut, (size_t)V * sizeof(double));
+    if (khat) memcpy(khat + (size_t)t * K, kh, (size_t)K * sizeof(double));
+    if (alpha) memcpy(alpha + (size_t)t * K, al, (size_t)K * sizeof(double));
+    if (states) memcpy(states + (size_t)t * VK, S, VK * sizeof(double));
+  }
+  free(S); free(kh); free(qh); free(al); free(ut); free(ot);
+}
+
+/* Forward replay of n recorded KDA tokens on S[V][K], in place:
+ * S[i][j] = alpha_t[j] * S[i][j] + u_t[i] khat_t[j], t = 0..n-1. */
+void gdn_oracle_kda_replay(int K, int V, int n, double* S, const double* u,
+                           const double* khat, const double* alpha) {
+  for (int t = 0; t < n; ++t) {
+    const double* ut = u + (size_t)t * V;
+    const double* kt = khat + (size_t)t * K;
+    const double* at = alpha + (size_t)t * K;
+    for (int i = 0; i < V; ++i)
+      for (int j = 0; j < K; ++j) {
+        double h = S[(size_t)i * K + j] * at[j];
+        S[(size_t)i * K + j] = h + ut[i] * kt[j];
+      }
+  }
+}
+
+/* KDA verify (and, when snaps != NULL, native snapshots) of one layer.
+ * As gdn_oracle_spec_verify, except a [T][HV][K], dt_bias [HV][K] and
+ * rec_g [B][HV][W_max][K]. */
+int gdn_oracle_kda_spec_verify(int HK, int HV, int K, int V, int W_max, int B,
+                               int T, int num_slots, const double* q,
+                               const double* k, const double* v,
+                               const double* a, const double* b,
+                               const double* A_log, const double* dt_bias,
+                               const int32_t* token_start,
+                               const int32_t* window_len, const double* pool,
+                               const int32_t* slot_table, int table_stride,
+                               const int32_t* seq_pos, int block_size,
+                               double* out, double* rec_u, double* rec_k,
+                               double* rec_g, double* snaps, int32_t* row_err) {
+  if (HK <= 0 || HV <= 0 || HV % HK != 0 || K <= 0 || V <= 0 || W_max <= 0)
+    return -2;
+  int group = HV / HK;
+  size_t VK = (size_t)V * K;
+  for (int r = 0; r < B; ++r) row_err[r] = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long unit = 0; unit < (long)B * HV; ++unit) {
+    int r = (int)(unit / HV), h = (int)(unit % HV);
+    int w = window_len[r];
+    int sp = seq_pos ? seq_pos[r] : 0;
+    int src = gdn_oracle_source_slot(w, slot_table + (size_t)r * table_stride,
+                                     table_stride, sp, block_size, num_slots,
+                                     W_max);
+    int err = src < -1 ? -src - 1 : 0;
+    long t0 = token_start[r];
+    if (!err && w > 0 && src >= 0 && (t0 < 0 || t0 + w > T))
+      err = ORACLE_ERR_TOKENS;
+    if (err) { if (h == 0) row_err[r] = err; continue; }
+    if (src < 0 || w == 0) continue;
+    int hk = h / group;
+    double* qa = (double*)malloc((size_t)w * K * sizeof(double));
+    double* ka = (double*)malloc((size_t)w * K * sizeof(double));
+    double* va = (double*)malloc((size_t)w * V * sizeof(double));
+    double* aa = (double*)malloc((size_t)w * K * sizeof(double));
+    double* ba = (double*)malloc((size_t)w * sizeof(double));
+    double* oa = (double*)malloc((size_t)w * V * sizeof(double));
+    double* ua = (double*)malloc((size_t)w * V * sizeof(double));
+    double* kh = (double*)malloc((size_t)w * K * sizeof(double));
+    double* ga = (double*)malloc((size_t)w * K * sizeof(double));
+    double* st = snaps ? (double*)malloc((size_t)w * VK * sizeof(double)) : NULL;
+    for (int t = 0; t < w; ++t) {
+      long row = t0 + t;
+      memcpy(qa + (size_t)t * K, q + ((size_t)row * HK + hk) * K, (size_t)K * sizeof(double));
+      memcpy(ka + (size_t)t * K, k + ((size_t)row * HK + hk) * K, (size_t)K * sizeof(double));
+      memcpy(va + (size_t)t * V, v + ((size_t)row * HV + h) * V, (size_t)V * sizeof(double));
+      memcpy(aa + (size_t)t * K, a + ((size_t)row * HV + h) * K, (size_t)K * sizeof(double));
+      ba[t] = b[(size_t)row * HV + h];
+    }
+    const double* S0 = pool + ((size_t)src * HV + h) * VK;
+    gdn_oracle_kda_window(K, V, w, S0, qa, ka, va, aa, ba, A_log[h],
+                          dt_bias + (size_t)h * K, oa, ua, kh, ga, st);
+    for (int t = 0; t < w; ++t) {
+      long row = t0 + t;
+      if (out)
+        memcpy(out + ((size_t)row * HV + h) * V, oa + (size_t)t * V, (size_t)V * sizeof(double));
+      size_t rec = ((size_t)r * HV + h) * W_max + t;
+      if (rec_u) memcpy(rec_u + rec * V, ua + (size_t)t * V, (size_t)V * sizeof(double));
+      if (rec_k) memcpy(rec_k + rec * K, kh + (size_t)t * K, (size_t)K * sizeof(double));
+      if (rec_g) memcpy(rec_g + rec * K, ga + (size_t)t * K, (size_t)K * sizeof(double));
+      if (snaps)
+        memcpy(snaps + (((size_t)r * W_max + t) * HV + h) * VK, st + (size_t)t * VK,
+               VK * sizeof(double));
+    }
+    free(qa); free(ka); free(va); free(aa); free(ba);
+    free(oa); free(ua); free(kh); free(ga); free(st);
+  }
+  return 0;
+}
+
+/* All-layer KDA replay commit from records (one slot table for every
+ * layer).  As gdn_oracle_replay_commit, except rec_g [L][B][HV][W_max][K]:
+ * every fold reads its source from pools_in, so the result does not depend
+ * on the order of the writes. */
+int gdn_oracle_kda_replay_commit(int L, int HV, int K, int V, int W_max, int B,
+                                 int num_slots, const double* pools_in,
+                                 double* pools_out, const double* rec_u,
+                                 const double* rec_k, const double* rec_g,
+                                 const int32_t* window_len,
+                                 const int32_t* accepted_len,
+                                 const int32_t* slot_table, int table_stride,
+                                 const int32_t* seq_pos, int block_size,
+                                 int32_t* row_err) {
+  if (L <= 0 || HV <= 0 || K <= 0 || V <= 0 || W_max <= 0) return -2;
+  size_t VK = (size_t)V * K;
+  size_t pool_elems = (size_t)num_slots * HV * VK;
+  int max_writes = 2 + W_max;
+  for (int r = 0; r < B; ++r) {
+    int32_t src, slots[64], ntok[64];
+    int sp = seq_pos ? seq_pos[r] : 0;
+    int nw = gdn_oracle_commit_plan(window_len[r], accepted_len[r],
+                                    slot_table + (size_t)r * table_stride,
+                                    table_stride, sp, block_size, num_slots,
+                                    W_max, &src, slots, ntok, max_writes);
+    row_err[r] = nw < 0 ? -nw - 1 : 0;
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long unit = 0; unit < (long)L * B * HV; ++unit) {
+    int l = (int)(unit / ((long)B * HV));
+    int r = (int)((unit / HV) % B);
+    int h = (int)(unit % HV);
+    int32_t src, slots[64], ntok[64];
+    int sp = seq_pos ? seq_pos[r] : 0;
+    int nw = gdn_oracle_commit_plan(window_len[r], accepted_len[r],
+                                    slot_table + (size_t)r * table_stride,
+                                    table_stride, sp, block_size, num_slots,
+                                    W_max, &src, slots, ntok, max_writes);
+    if (nw <= 0) continue;
+    size_t rec = (((size_t)l * B + r) * HV + h) * W_max;
+    double* S = (double*)malloc(VK * sizeof(double));
+    for (int i = 0; i < nw; ++i) {
+      memcpy(S, pools_in + l * pool_elems + ((size_t)src * HV + h) * VK,
+             VK * sizeof(double));
+      gdn_oracle_kda_replay(K, V, ntok[i], S, rec_u + rec * V, rec_k + rec * K,
+                            rec_g + rec * K);
+      memcpy(pools_out + l * pool_elems + ((size_t)slots[i] * HV + h) * VK, S,
+             VK * sizeof(double));
+    }
+    free(S);
+  }
+  return 0;
+}

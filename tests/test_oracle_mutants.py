@@ -2,7 +2,7 @@
 
 Each case plants one mistake in a temporary copy of ``oracle/gdn_oracle.c``
 (on the CPU), rebuilds it there and runs ``test_oracle_pins.py`` against the
-copy; the pin suite has to fail.
+copy; the pin suites (scalar gate and per-channel KDA gate) have to fail.
 """
 import os
 import shutil
@@ -36,6 +36,19 @@ MUTANTS = {
     "boundary_fold_reads_written_pool": (
         "memcpy(S, pools_in + l * pool_elems + ((size_t)src * HV + h) * VK,",
         "memcpy(S, pools_out + l * pool_elems + ((size_t)src * HV + h) * VK,"),
+    "kda_decay_along_value_rows": (
+        "for (int j = 0; j < K; ++j) S[(size_t)i * K + j] *= alpha[j];",
+        "for (int j = 0; j < K; ++j) S[(size_t)i * K + j] *= alpha[i % K];"),
+    "kda_replay_decay_along_value_rows": ("double h = S[(size_t)i * K + j] * at[j];",
+                                          "double h = S[(size_t)i * K + j] * at[i % K];"),
+    "kda_bias_per_head_not_channel": (
+        "al[j] = gdn_oracle_decay(a[(size_t)t * K + j], A_log, dt_bias[j]);",
+        "al[j] = gdn_oracle_decay(a[(size_t)t * K + j], A_log, dt_bias[0]);"),
+    "kda_gate_ignores_head": ("memcpy(aa + (size_t)t * K, a + ((size_t)row * HV + h) * K,",
+                              "memcpy(aa + (size_t)t * K, a + ((size_t)row * HV) * K,"),
+    "kda_record_keeps_first_gate": (
+        "memcpy(rec_g + rec * K, ga + (size_t)t * K, (size_t)K * sizeof(double));",
+        "memcpy(rec_g + rec * K, ga, (size_t)K * sizeof(double));"),
     "source_one_token_late": (
         "int32_t s = slot_after(table_row, table_stride, block_size, seq_pos);",
         "int32_t s = slot_after(table_row, table_stride, block_size, seq_pos + 1);"),
@@ -57,6 +70,6 @@ def test_pins_catch_mutant(name, tmp_path):
     for f in ("__init__.py", "workloads.py"):
         shutil.copy(os.path.join(ROOT, "spec_decode_recurrent_gb300", f), pkg / f)
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py"], cwd=tmp_path, capture_output=True,
-                       text=True, timeout=300)
+                        "tests/test_oracle_pins.py", "tests/test_oracle_kda_pins.py"],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
