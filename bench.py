@@ -59,6 +59,10 @@ DESCR = {
                    "non-contiguous rows, strided fused q/k/v, gates U(-20,20), 512-slot pools, seed 30",
     "align": "36 GDN layers, batch 128, window 4, align mode with block size 4, boundary "
              "slot often equal to the source slot, 384-slot pools, seed 4",
+    "kda_all_layer": "all_layer shapes (36 layers, batch 64 with 8 padding rows, HK=16 HV=32 "
+                     "K=V=128, window 4) with the per-channel (KDA) decay: gate inputs "
+                     "a [T,HV,K] ~ N(0,1), dt_bias [HV,K] ~ U(-1,1), gate records [B,HV,W,K], "
+                     "seed 6",
 }
 
 
@@ -86,7 +90,8 @@ def parse(argv=None):
     return p.parse_args(argv)
 
 
-DEFAULT_SEED = {"tiny": 0, "all_layer": 2, "layer": 1, "long_ragged": 30, "align": 4, "mtp5": 5}
+DEFAULT_SEED = {"tiny": 0, "all_layer": 2, "layer": 1, "long_ragged": 30, "align": 4, "mtp5": 5,
+                "kda_all_layer": 6}
 
 
 def make_workload(name, device, rank, state_dtype, layers=None, seed=None):
@@ -472,6 +477,7 @@ CONFIGS = [
     ("long_ragged_seed32", "long_ragged", "f32", 32),
     ("align_fp32", "align", "f32", None),
     ("align_bf16", "align", "bf16", None),
+    ("kda_all_layer", "kda_all_layer", "f32", None),
 ]
 
 

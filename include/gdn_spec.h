@@ -280,6 +280,61 @@ int gdn_native_spec_snapshot(
     float* out, int64_t out_row_stride, void* snapshots, int32_t* err,
     void* stream);
 
+/*
+ * Per-channel decay (KDA) variant of the three calls above.  The pages
+ * name KDA as the layer the verify/commit protocol was first built for
+ * (tokenspeed PR above, Summary; vLLM PR above, Purpose) but print no KDA
+ * formula; the reading implemented here replaces the scalar decay by a
+ * vector over the K key channels and changes nothing else:
+ *   alpha_t[j] = exp(-exp(A_log[h]) * softplus(a[t,h,j] + dt_bias[h,j]))
+ *   H = S diag(alpha_t)   (column j of the [V][K] state scaled by alpha_t[j])
+ *   u_t = beta_t * (v_t - H khat_t);  S = H + u_t khat_t^T;  o_t = S qhat_t
+ * and the replay record keeps the whole gate vector.  The commit's fold is
+ * S[i][j] = fma(u[i], khat[j], S[i][j] * alpha[j]), so, as for the scalar
+ * gate, verify == native and commit(n) == native snapshot n bit for bit.
+ *
+ * Arguments exactly as gdn_spec_verify / gdn_native_spec_snapshot /
+ * gdn_replay_commit, except these layouts:
+ *   a             [num_tokens][HV][K] fp32, contiguous: per-channel raw gates.
+ *   dt_bias       [HV][K] fp32.
+ *   rec_g         [batch][HV][W][K] fp32, 16-byte aligned (verify output,
+ *                 commit input through its pointer array): the gate vector
+ *                 of token t of row r in position t.  The reject marker is
+ *                 rec_g[r][h][0][0] = -1.0.
+ */
+int gdn_kda_spec_verify(const gdn_shape* shape, int32_t batch, int32_t num_tokens,
+                        int32_t num_slots, const void* q, int64_t q_row_stride,
+                        const void* k, int64_t k_row_stride, const void* v,
+                        int64_t v_row_stride, const float* a, const float* b,
+                        const float* A_log, const float* dt_bias,
+                        const int32_t* token_start, const int32_t* window_len,
+                        const void* state_pool, const int32_t* slot_table,
+                        int32_t slot_table_stride, const int32_t* seq_pos,
+                        int32_t block_size, float* out, int64_t out_row_stride,
+                        float* rec_u, float* rec_k, float* rec_g, int32_t* err,
+                        void* stream);
+
+int gdn_kda_native_spec_snapshot(
+    const gdn_shape* shape, int32_t batch, int32_t num_tokens,
+    int32_t num_slots, const void* q, int64_t q_row_stride, const void* k,
+    int64_t k_row_stride, const void* v, int64_t v_row_stride, const float* a,
+    const float* b, const float* A_log, const float* dt_bias,
+    const int32_t* token_start, const int32_t* window_len,
+    const void* state_pool, const int32_t* slot_table,
+    int32_t slot_table_stride, const int32_t* seq_pos, int32_t block_size,
+    float* out, int64_t out_row_stride, void* snapshots, int32_t* err,
+    void* stream);
+
+int gdn_kda_replay_commit(const gdn_shape* shape, int32_t num_layers,
+                          int32_t batch, int32_t num_slots,
+                          void* const* state_pools, const float* const* rec_u,
+                          const float* const* rec_k, const float* const* rec_g,
+                          const int32_t* window_len,
+                          const int32_t* accepted_len,
+                          const int32_t* slot_table, int32_t slot_table_stride,
+                          const int32_t* seq_pos, int32_t block_size,
+                          int32_t* err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,8 @@ ROW_ERR_WINDOW, ROW_ERR_ACCEPTED, ROW_ERR_SLOT = 1, 2, 4
 ROW_ERR_BLOCK, ROW_ERR_SEQPOS, ROW_ERR_TOKENS = 8, 16, 32
 ROW_ERR_GROUP, ROW_ERR_REJECTED = 64, 128
 ENTRY_POINTS = ("gdn_spec_verify", "gdn_replay_commit", "gdn_replay_commit_grouped",
-                "gdn_conv_state_commit", "gdn_native_spec_snapshot")
+                "gdn_conv_state_commit", "gdn_native_spec_snapshot", "gdn_kda_spec_verify",
+                "gdn_kda_native_spec_snapshot", "gdn_kda_replay_commit")
 
 _ERRORS = {-1: "null pointer", -2: "unsupported shape or dtype",
            -3: "invalid count, stride, alignment or block size", -4: "CUDA launch failed"}
@@ -70,6 +71,12 @@ def load() -> ctypes.CDLL:
             lib.gdn_replay_commit.argtypes = [ctypes.POINTER(gdn_shape), _I32, _I32, _I32,
                                               _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32,
                                               _P, _P]
+            lib.gdn_kda_spec_verify.restype = ctypes.c_int
+            lib.gdn_kda_spec_verify.argtypes = lib.gdn_spec_verify.argtypes
+            lib.gdn_kda_native_spec_snapshot.restype = ctypes.c_int
+            lib.gdn_kda_native_spec_snapshot.argtypes = lib.gdn_native_spec_snapshot.argtypes
+            lib.gdn_kda_replay_commit.restype = ctypes.c_int
+            lib.gdn_kda_replay_commit.argtypes = lib.gdn_replay_commit.argtypes
             lib.gdn_conv_state_commit.restype = ctypes.c_int
             lib.gdn_conv_state_commit.argtypes = [
                 _I32, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _I64, _P, _P,
@@ -120,7 +127,7 @@ def _contig(t: torch.Tensor, name: str, dtype):
 
 
 def _verify_args(q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_pool,
-                 slot_table, seq_pos, block_size, out, max_window):
+                 slot_table, seq_pos, block_size, out, max_window, kda=False):
     T, HK, K = q.shape
     _need(k.shape == q.shape and k.dtype == q.dtype, "k must match q")
     _need(v.shape[0] == T and v.dtype == q.dtype, "v must have q's rows and dtype")
@@ -130,12 +137,17 @@ def _verify_args(q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_p
     _need(out.shape == (T, HV, V), "out must be [num_tokens, HV, V]")
     _need(state_pool.dim() == 4 and state_pool.shape[1:] == (HV, V, K), "pool must be [slots, HV, V, K]")
     _contig(state_pool, "state_pool", state_pool.dtype)
-    for name, t, n in (("a", a, None), ("b", b, None)):
-        _contig(t, name, torch.float32)
-        _need(t.shape == (T, HV), f"{name} must be [num_tokens, HV]")
-    for name, t in (("A_log", A_log), ("dt_bias", dt_bias)):
-        _contig(t, name, torch.float32)
-        _need(t.numel() == HV, f"{name} must have HV entries")
+    # per-channel (KDA) gates: a [T, HV, K] and dt_bias [HV, K]
+    G = K if kda else 1
+    _contig(a, "a", torch.float32)
+    _need(a.numel() == T * HV * G and a.shape[:2] == (T, HV),
+          "a must be [num_tokens, HV]" + (", K]" if kda else ""))
+    _contig(b, "b", torch.float32)
+    _need(b.shape == (T, HV), "b must be [num_tokens, HV]")
+    _contig(A_log, "A_log", torch.float32)
+    _need(A_log.numel() == HV, "A_log must have HV entries")
+    _contig(dt_bias, "dt_bias", torch.float32)
+    _need(dt_bias.numel() == HV * G, "dt_bias must have HV" + (" * K" if kda else "") + " entries")
     B = window_len.shape[0]
     for name, t in (("token_start", token_start), ("window_len", window_len)):
         _contig(t, name, torch.int32)
@@ -154,41 +166,74 @@ def _verify_args(q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_p
     return shape, head, B, HV, V, K
 
 
-def gdn_spec_verify(*, q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_pool,
-                    slot_table, out, rec_u, rec_k, rec_g, max_window, seq_pos=None,
-                    block_size=0, err=None, stream=None) -> None:
-    """Verify one layer: writes out and the replay record, never the pool."""
+def _verify(fn, kda, q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+            slot_table, out, rec_u, rec_k, rec_g, max_window, seq_pos, block_size, err, stream):
     shape, head, B, HV, V, K = _verify_args(q, k, v, a, b, A_log, dt_bias, token_start,
                                             window_len, state_pool, slot_table, seq_pos,
-                                            block_size, out, max_window)
+                                            block_size, out, max_window, kda)
     W = int(max_window)
     for name, t, shp in (("rec_u", rec_u, (B, HV, W, V)), ("rec_k", rec_k, (B, HV, W, K)),
-                         ("rec_g", rec_g, (B, HV, W))):
+                         ("rec_g", rec_g, (B, HV, W, K) if kda else (B, HV, W))):
         _contig(t, name, torch.float32)
         _need(tuple(t.shape) == shp, f"{name} must be {shp}")
     if err is not None:
         _contig(err, "err", torch.int32)
-    rc = load().gdn_spec_verify(*head, _ptr(rec_u), _ptr(rec_k), _ptr(rec_g), _ptr(err),
-                                _stream(stream))
+    rc = getattr(load(), fn)(*head, _ptr(rec_u), _ptr(rec_k), _ptr(rec_g), _ptr(err),
+                             _stream(stream))
     if rc != 0:
-        raise GDNError("gdn_spec_verify", rc)
+        raise GDNError(fn, rc)
+
+
+def _native(fn, kda, q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+            slot_table, out, snapshots, max_window, seq_pos, block_size, err, stream):
+    shape, head, B, HV, V, K = _verify_args(q, k, v, a, b, A_log, dt_bias, token_start,
+                                            window_len, state_pool, slot_table, seq_pos,
+                                            block_size, out, max_window, kda)
+    W = int(max_window)
+    _contig(snapshots, "snapshots", state_pool.dtype)
+    _need(tuple(snapshots.shape) == (B, W, HV, V, K), "snapshots must be [batch, W, HV, V, K]")
+    if err is not None:
+        _contig(err, "err", torch.int32)
+    rc = getattr(load(), fn)(*head, _ptr(snapshots), _ptr(err), _stream(stream))
+    if rc != 0:
+        raise GDNError(fn, rc)
+
+
+def gdn_spec_verify(*, q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+                    slot_table, out, rec_u, rec_k, rec_g, max_window, seq_pos=None,
+                    block_size=0, err=None, stream=None) -> None:
+    """Verify one layer: writes out and the replay record, never the pool."""
+    _verify("gdn_spec_verify", False, q, k, v, a, b, A_log, dt_bias, token_start, window_len,
+            state_pool, slot_table, out, rec_u, rec_k, rec_g, max_window, seq_pos, block_size,
+            err, stream)
+
+
+def gdn_kda_spec_verify(*, q, k, v, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+                        slot_table, out, rec_u, rec_k, rec_g, max_window, seq_pos=None,
+                        block_size=0, err=None, stream=None) -> None:
+    """Per-channel-decay (KDA) verify of one layer: a [T, HV, K], dt_bias
+    [HV, K], rec_g [B, HV, W, K]; otherwise as gdn_spec_verify."""
+    _verify("gdn_kda_spec_verify", True, q, k, v, a, b, A_log, dt_bias, token_start, window_len,
+            state_pool, slot_table, out, rec_u, rec_k, rec_g, max_window, seq_pos, block_size,
+            err, stream)
 
 
 def gdn_native_spec_snapshot(*, q, k, v, a, b, A_log, dt_bias, token_start, window_len,
                              state_pool, slot_table, out, snapshots, max_window, seq_pos=None,
                              block_size=0, err=None, stream=None) -> None:
     """Native baseline of one layer: writes out and the state after every token."""
-    shape, head, B, HV, V, K = _verify_args(q, k, v, a, b, A_log, dt_bias, token_start,
-                                            window_len, state_pool, slot_table, seq_pos,
-                                            block_size, out, max_window)
-    W = int(max_window)
-    _contig(snapshots, "snapshots", state_pool.dtype)
-    _need(tuple(snapshots.shape) == (B, W, HV, V, K), "snapshots must be [batch, W, HV, V, K]")
-    if err is not None:
-        _contig(err, "err", torch.int32)
-    rc = load().gdn_native_spec_snapshot(*head, _ptr(snapshots), _ptr(err), _stream(stream))
-    if rc != 0:
-        raise GDNError("gdn_native_spec_snapshot", rc)
+    _native("gdn_native_spec_snapshot", False, q, k, v, a, b, A_log, dt_bias, token_start,
+            window_len, state_pool, slot_table, out, snapshots, max_window, seq_pos, block_size,
+            err, stream)
+
+
+def gdn_kda_native_spec_snapshot(*, q, k, v, a, b, A_log, dt_bias, token_start, window_len,
+                                 state_pool, slot_table, out, snapshots, max_window,
+                                 seq_pos=None, block_size=0, err=None, stream=None) -> None:
+    """Native baseline of one layer with the per-channel (KDA) decay."""
+    _native("gdn_kda_native_spec_snapshot", True, q, k, v, a, b, A_log, dt_bias, token_start,
+            window_len, state_pool, slot_table, out, snapshots, max_window, seq_pos, block_size,
+            err, stream)
 
 
 class LayerTable:
@@ -214,12 +259,14 @@ class LayerTable:
         self.num_slots, self.HV, self.V, self.K = p0.shape
         self.state_dtype = p0.dtype
         self.B, _, self.W, _ = rec_u[0].shape
+        self.kda = rec_g[0].dim() == 4        # per-channel gate records [B, HV, W, K]
 
 
 def gdn_replay_commit(*, table: LayerTable, num_k_heads: int, window_len, accepted_len,
                       slot_table, seq_pos=None, block_size=0, err=None, stream=None) -> None:
     """All-layer commit in one launch: replays the accepted prefix of every
-    row of every layer and writes each state once (plus align boundaries)."""
+    row of every layer and writes each state once (plus align boundaries).
+    A table of per-channel gate records (KDA) calls gdn_kda_replay_commit."""
     B = window_len.shape[0]
     _need(B == table.B, "batch must match the record buffers")
     for name, t in (("window_len", window_len), ("accepted_len", accepted_len)):
@@ -234,13 +281,14 @@ def gdn_replay_commit(*, table: LayerTable, num_k_heads: int, window_len, accept
     # the commit reads no q/k/v: qkv_dtype is a placeholder
     shape = gdn_shape(int(num_k_heads), table.HV, table.K, table.V, table.W, GDN_DTYPE_F32,
                       _dtype_code(table.state_dtype))
-    rc = load().gdn_replay_commit(
+    fn = "gdn_kda_replay_commit" if table.kda else "gdn_replay_commit"
+    rc = getattr(load(), fn)(
         ctypes.byref(shape), table.num_layers, B, table.num_slots, _ptr(table.d_pools),
         _ptr(table.d_rec_u), _ptr(table.d_rec_k), _ptr(table.d_rec_g), _ptr(window_len),
         _ptr(accepted_len), _ptr(st), st.shape[1], _ptr(seq_pos if block_size else None),
         int(block_size), _ptr(err), _stream(stream))
     if rc != 0:
-        raise GDNError("gdn_replay_commit", rc)
+        raise GDNError(fn, rc)
 
 
 def gdn_replay_commit_grouped(*, table: LayerTable, num_k_heads: int, layer_group, window_len,
@@ -248,6 +296,7 @@ def gdn_replay_commit_grouped(*, table: LayerTable, num_k_heads: int, layer_grou
                               stream=None) -> None:
     """All-layer commit in one launch for layers split into KV-cache groups:
     layer l uses slot_tables[layer_group[l]] ([groups, batch, stride])."""
+    _need(not table.kda, "the grouped commit takes scalar-gate records")
     B = window_len.shape[0]
     _need(B == table.B, "batch must match the record buffers")
     for name, t in (("window_len", window_len), ("accepted_len", accepted_len)):

@@ -91,21 +91,14 @@ int prepare_verify(gdn::VerifyParams* p, const gdn_shape* s, int32_t batch,
   return GDN_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int gdn_spec_verify(const gdn_shape* shape, int32_t batch, int32_t num_tokens,
-                    int32_t num_slots, const void* q, int64_t q_row_stride,
-                    const void* k, int64_t k_row_stride, const void* v,
-                    int64_t v_row_stride, const float* a, const float* b,
-                    const float* A_log, const float* dt_bias,
-                    const int32_t* token_start, const int32_t* window_len,
-                    const void* state_pool, const int32_t* slot_table,
-                    int32_t slot_table_stride, const int32_t* seq_pos,
-                    int32_t block_size, float* out, int64_t out_row_stride,
-                    float* rec_u, float* rec_k, float* rec_g, int32_t* err,
-                    void* stream) {
+int verify_common(const gdn_shape* shape, int32_t batch, int32_t num_tokens, int32_t num_slots,
+                  const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                  const void* v, int64_t v_row_stride, const float* a, const float* b,
+                  const float* A_log, const float* dt_bias, const int32_t* token_start,
+                  const int32_t* window_len, const void* state_pool, const int32_t* slot_table,
+                  int32_t slot_table_stride, const int32_t* seq_pos, int32_t block_size,
+                  float* out, int64_t out_row_stride, float* rec_u, float* rec_k, float* rec_g,
+                  void* snapshots, int32_t* err, void* stream, bool native, bool kda) {
   if (batch == 0) return check_shape(shape);  // nothing to do; row arrays may be empty
   gdn::VerifyParams p;
   int rc = prepare_verify(&p, shape, batch, num_tokens, num_slots, q, q_row_stride, k,
@@ -113,49 +106,31 @@ int gdn_spec_verify(const gdn_shape* shape, int32_t batch, int32_t num_tokens,
                           window_len, state_pool, slot_table, slot_table_stride, seq_pos,
                           block_size, out, out_row_stride);
   if (rc != GDN_OK) return rc;
-  if (!rec_u || !rec_k || !rec_g) return GDN_ERR_NULL;
-  if (!aligned(rec_u, 16) || !aligned(rec_k, 16) || !aligned(rec_g, 4)) return GDN_ERR_INVALID;
-  if (batch == 0) return GDN_OK;
-  p.rec_u = rec_u;
-  p.rec_k = rec_k;
-  p.rec_g = rec_g;
+  if (native) {
+    if (!snapshots) return GDN_ERR_NULL;
+    if (!aligned(snapshots, 16)) return GDN_ERR_INVALID;
+    p.snaps = snapshots;
+  } else {
+    if (!rec_u || !rec_k || !rec_g) return GDN_ERR_NULL;
+    // a per-channel gate record moves in 16-byte pieces
+    if (!aligned(rec_u, 16) || !aligned(rec_k, 16) || !aligned(rec_g, kda ? 16 : 4))
+      return GDN_ERR_INVALID;
+    p.rec_u = rec_u;
+    p.rec_k = rec_k;
+    p.rec_g = rec_g;
+  }
   p.err = err;
-  return gdn::launch_verify(p, shape->head_k, shape->qkv_dtype, shape->state_dtype, false,
+  return gdn::launch_verify(p, shape->head_k, shape->qkv_dtype, shape->state_dtype, native, kda,
                             static_cast<cudaStream_t>(stream));
 }
 
-int gdn_native_spec_snapshot(
-    const gdn_shape* shape, int32_t batch, int32_t num_tokens, int32_t num_slots,
-    const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
-    int64_t v_row_stride, const float* a, const float* b, const float* A_log,
-    const float* dt_bias, const int32_t* token_start, const int32_t* window_len,
-    const void* state_pool, const int32_t* slot_table, int32_t slot_table_stride,
-    const int32_t* seq_pos, int32_t block_size, float* out, int64_t out_row_stride,
-    void* snapshots, int32_t* err, void* stream) {
-  if (batch == 0) return check_shape(shape);
-  gdn::VerifyParams p;
-  int rc = prepare_verify(&p, shape, batch, num_tokens, num_slots, q, q_row_stride, k,
-                          k_row_stride, v, v_row_stride, a, b, A_log, dt_bias, token_start,
-                          window_len, state_pool, slot_table, slot_table_stride, seq_pos,
-                          block_size, out, out_row_stride);
-  if (rc != GDN_OK) return rc;
-  if (!snapshots) return GDN_ERR_NULL;
-  if (!aligned(snapshots, 16)) return GDN_ERR_INVALID;
-  if (batch == 0) return GDN_OK;
-  p.snaps = snapshots;
-  p.err = err;
-  return gdn::launch_verify(p, shape->head_k, shape->qkv_dtype, shape->state_dtype, true,
-                            static_cast<cudaStream_t>(stream));
-}
-
-int gdn_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers, int32_t num_groups,
-                              const int32_t* layer_group, int32_t batch, int32_t num_slots,
-                              void* const* state_pools, const float* const* rec_u,
-                              const float* const* rec_k, const float* const* rec_g,
-                              const int32_t* window_len, const int32_t* accepted_len,
-                              const int32_t* slot_tables, int32_t slot_table_stride,
-                              int64_t group_stride, const int32_t* seq_pos, int32_t block_size,
-                              int32_t* err, void* stream) {
+int commit_common(const gdn_shape* shape, int32_t num_layers, int32_t num_groups,
+                  const int32_t* layer_group, int32_t batch, int32_t num_slots,
+                  void* const* state_pools, const float* const* rec_u, const float* const* rec_k,
+                  const float* const* rec_g, const int32_t* window_len,
+                  const int32_t* accepted_len, const int32_t* slot_tables,
+                  int32_t slot_table_stride, int64_t group_stride, const int32_t* seq_pos,
+                  int32_t block_size, int32_t* err, void* stream, bool kda) {
   int rc = check_shape(shape);
   if (rc != GDN_OK || batch == 0) return rc;
   if (!state_pools || !rec_u || !rec_k || !rec_g || !window_len || !accepted_len ||
@@ -189,8 +164,86 @@ int gdn_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers, int32_
   p.seq_pos = seq_pos;
   p.block_size = block_size;
   p.err = err;
-  return gdn::launch_commit(p, shape->head_k, shape->state_dtype,
+  return gdn::launch_commit(p, shape->head_k, shape->state_dtype, kda,
                             static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_spec_verify(const gdn_shape* shape, int32_t batch, int32_t num_tokens,
+                    int32_t num_slots, const void* q, int64_t q_row_stride,
+                    const void* k, int64_t k_row_stride, const void* v,
+                    int64_t v_row_stride, const float* a, const float* b,
+                    const float* A_log, const float* dt_bias,
+                    const int32_t* token_start, const int32_t* window_len,
+                    const void* state_pool, const int32_t* slot_table,
+                    int32_t slot_table_stride, const int32_t* seq_pos,
+                    int32_t block_size, float* out, int64_t out_row_stride,
+                    float* rec_u, float* rec_k, float* rec_g, int32_t* err,
+                    void* stream) {
+  return verify_common(shape, batch, num_tokens, num_slots, q, q_row_stride, k, k_row_stride, v,
+                       v_row_stride, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+                       slot_table, slot_table_stride, seq_pos, block_size, out, out_row_stride,
+                       rec_u, rec_k, rec_g, nullptr, err, stream, false, false);
+}
+
+int gdn_native_spec_snapshot(
+    const gdn_shape* shape, int32_t batch, int32_t num_tokens, int32_t num_slots,
+    const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+    int64_t v_row_stride, const float* a, const float* b, const float* A_log,
+    const float* dt_bias, const int32_t* token_start, const int32_t* window_len,
+    const void* state_pool, const int32_t* slot_table, int32_t slot_table_stride,
+    const int32_t* seq_pos, int32_t block_size, float* out, int64_t out_row_stride,
+    void* snapshots, int32_t* err, void* stream) {
+  return verify_common(shape, batch, num_tokens, num_slots, q, q_row_stride, k, k_row_stride, v,
+                       v_row_stride, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+                       slot_table, slot_table_stride, seq_pos, block_size, out, out_row_stride,
+                       nullptr, nullptr, nullptr, snapshots, err, stream, true, false);
+}
+
+int gdn_kda_spec_verify(const gdn_shape* shape, int32_t batch, int32_t num_tokens,
+                        int32_t num_slots, const void* q, int64_t q_row_stride, const void* k,
+                        int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                        const float* a, const float* b, const float* A_log,
+                        const float* dt_bias, const int32_t* token_start,
+                        const int32_t* window_len, const void* state_pool,
+                        const int32_t* slot_table, int32_t slot_table_stride,
+                        const int32_t* seq_pos, int32_t block_size, float* out,
+                        int64_t out_row_stride, float* rec_u, float* rec_k, float* rec_g,
+                        int32_t* err, void* stream) {
+  return verify_common(shape, batch, num_tokens, num_slots, q, q_row_stride, k, k_row_stride, v,
+                       v_row_stride, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+                       slot_table, slot_table_stride, seq_pos, block_size, out, out_row_stride,
+                       rec_u, rec_k, rec_g, nullptr, err, stream, false, true);
+}
+
+int gdn_kda_native_spec_snapshot(
+    const gdn_shape* shape, int32_t batch, int32_t num_tokens, int32_t num_slots,
+    const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+    int64_t v_row_stride, const float* a, const float* b, const float* A_log,
+    const float* dt_bias, const int32_t* token_start, const int32_t* window_len,
+    const void* state_pool, const int32_t* slot_table, int32_t slot_table_stride,
+    const int32_t* seq_pos, int32_t block_size, float* out, int64_t out_row_stride,
+    void* snapshots, int32_t* err, void* stream) {
+  return verify_common(shape, batch, num_tokens, num_slots, q, q_row_stride, k, k_row_stride, v,
+                       v_row_stride, a, b, A_log, dt_bias, token_start, window_len, state_pool,
+                       slot_table, slot_table_stride, seq_pos, block_size, out, out_row_stride,
+                       nullptr, nullptr, nullptr, snapshots, err, stream, true, true);
+}
+
+int gdn_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers, int32_t num_groups,
+                              const int32_t* layer_group, int32_t batch, int32_t num_slots,
+                              void* const* state_pools, const float* const* rec_u,
+                              const float* const* rec_k, const float* const* rec_g,
+                              const int32_t* window_len, const int32_t* accepted_len,
+                              const int32_t* slot_tables, int32_t slot_table_stride,
+                              int64_t group_stride, const int32_t* seq_pos, int32_t block_size,
+                              int32_t* err, void* stream) {
+  return commit_common(shape, num_layers, num_groups, layer_group, batch, num_slots, state_pools,
+                       rec_u, rec_k, rec_g, window_len, accepted_len, slot_tables,
+                       slot_table_stride, group_stride, seq_pos, block_size, err, stream, false);
 }
 
 int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
@@ -200,9 +253,21 @@ int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
                       const int32_t* slot_table, int32_t slot_table_stride,
                       const int32_t* seq_pos, int32_t block_size, int32_t* err,
                       void* stream) {
-  return gdn_replay_commit_grouped(shape, num_layers, 1, nullptr, batch, num_slots, state_pools,
-                                   rec_u, rec_k, rec_g, window_len, accepted_len, slot_table,
-                                   slot_table_stride, 0, seq_pos, block_size, err, stream);
+  return commit_common(shape, num_layers, 1, nullptr, batch, num_slots, state_pools, rec_u,
+                       rec_k, rec_g, window_len, accepted_len, slot_table, slot_table_stride, 0,
+                       seq_pos, block_size, err, stream, false);
+}
+
+int gdn_kda_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
+                          int32_t num_slots, void* const* state_pools,
+                          const float* const* rec_u, const float* const* rec_k,
+                          const float* const* rec_g, const int32_t* window_len,
+                          const int32_t* accepted_len, const int32_t* slot_table,
+                          int32_t slot_table_stride, const int32_t* seq_pos, int32_t block_size,
+                          int32_t* err, void* stream) {
+  return commit_common(shape, num_layers, 1, nullptr, batch, num_slots, state_pools, rec_u,
+                       rec_k, rec_g, window_len, accepted_len, slot_table, slot_table_stride, 0,
+                       seq_pos, block_size, err, stream, true);
 }
 
 int gdn_conv_state_commit(int32_t num_layers, int32_t num_groups, const int32_t* layer_group,

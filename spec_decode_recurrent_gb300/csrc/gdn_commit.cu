@@ -104,18 +104,24 @@ struct Chunk<__nv_bfloat16> {
 };
 
 // Fold token t of a staged record into the thread's chunks.  u_s holds the
-// corrections of rows [row_base, row_base + u_stride) of each token.
-template <int K, typename ST, int M, int NT>
-__device__ __forceinline__ void fold_token(f32x2 (&x)[M][Chunk<ST>::E / 2], float alpha,
+// corrections of rows [row_base, row_base + u_stride) of each token; g_s
+// the gates, one per token ([W]) or, with the per-channel decay (KDA), one
+// vector per token ([W][K]) whose entries scale the matching columns.
+template <int K, typename ST, int M, int NT, bool KDA>
+__device__ __forceinline__ void fold_token(f32x2 (&x)[M][Chunk<ST>::E / 2], const float* g_s,
                                            const float* k_s, const float* u_s, int t,
                                            int u_stride, int col, int c0, int row_base,
                                            int nchunks) {
   constexpr int E = Chunk<ST>::E;
   constexpr int CPR = K / E;
-  const f32x2 al2 = pack2(alpha, alpha);
+  f32x2 al2[E / 2];
   f32x2 kk[E / 2];
 #pragma unroll
-  for (int e = 0; e < E / 2; ++e) kk[e] = *reinterpret_cast<const f32x2*>(k_s + t * K + col + 2 * e);
+  for (int e = 0; e < E / 2; ++e) {
+    kk[e] = *reinterpret_cast<const f32x2*>(k_s + t * K + col + 2 * e);
+    al2[e] = KDA ? *reinterpret_cast<const f32x2*>(g_s + t * K + col + 2 * e)
+                 : pack2(g_s[t], g_s[t]);
+  }
 #pragma unroll
   for (int m = 0; m < M; ++m) {
     const int c = c0 + NT * m;
@@ -123,7 +129,7 @@ __device__ __forceinline__ void fold_token(f32x2 (&x)[M][Chunk<ST>::E / 2], floa
       const float u = u_s[t * u_stride + c / CPR - row_base];
       const f32x2 u2 = pack2(u, u);
 #pragma unroll
-      for (int e = 0; e < E / 2; ++e) x[m][e] = fold2(x[m][e], al2, u2, kk[e]);
+      for (int e = 0; e < E / 2; ++e) x[m][e] = fold2(x[m][e], al2[e], u2, kk[e]);
     }
   }
 }
@@ -146,7 +152,7 @@ __device__ __forceinline__ void store_chunks(ST* dst, const f32x2 (&x)[M][Chunk<
 // waits only for the small record while the tile is still in flight.
 constexpr int kCommitThreads = 256;
 
-template <int K, typename ST, int M>
+template <int K, typename ST, int M, bool KDA>
 __global__ void __launch_bounds__(kCommitThreads)
     gdn_commit_kernel(const CommitParams p, int tiles_log2) {
   using C = Chunk<ST>;
@@ -177,16 +183,20 @@ __global__ void __launch_bounds__(kCommitThreads)
   // ---- alpha [n] (rows and K are multiples of 16: whole 16-byte pieces)
   float* u_s = smem;                     // [W][TILE_ROWS]
   float* k_s = u_s + p.W * TILE_ROWS;    // [W][K]
-  float* g_s = k_s + p.W * K;            // [W]
+  float* g_s = k_s + p.W * K;            // [W], or [W][K] for the per-channel gate
   const size_t rec = ((size_t)r * p.HV + h) * p.W;
   const float* ru = p.rec_u[layer] + rec * p.V + row_base;
   const float* rk = p.rec_k[layer] + rec * K;
-  const float* rg = p.rec_g[layer] + rec;
+  const float* rg = p.rec_g[layer] + rec * (KDA ? K : 1);
   const int urow4 = rows / 4;
   for (int i = tid; i < n * urow4; i += NT)
     cp_async16(u_s + (i / urow4) * TILE_ROWS + 4 * (i % urow4), ru + (size_t)(i / urow4) * p.V + 4 * (i % urow4));
   for (int i = tid; i < n * (K / 4); i += NT) cp_async16(k_s + 4 * i, rk + 4 * i);
-  if (tid < n) cp_async4(g_s + tid, rg + tid);
+  if constexpr (KDA) {
+    for (int i = tid; i < n * (K / 4); i += NT) cp_async16(g_s + 4 * i, rg + 4 * i);
+  } else {
+    if (tid < n) cp_async4(g_s + tid, rg + tid);
+  }
   cp_async_commit();
 
   // ---- then every chunk of the tile
@@ -210,7 +220,7 @@ __global__ void __launch_bounds__(kCommitThreads)
 
   const int col = (tid % CPR) * E;  // fixed column block of this thread
   for (int t = 0; t < n; ++t) {
-    fold_token<K, ST, M, NT>(x, g_s[t], k_s, u_s, t, TILE_ROWS, col, c0, row_base, nchunks);
+    fold_token<K, ST, M, NT, KDA>(x, g_s, k_s, u_s, t, TILE_ROWS, col, c0, row_base, nchunks);
     // align mode: the state after token p lands in slot(p) when p closes a block
     const long long pos = plan.p0 + t + 1;
     if (p.block_size > 0 && t + 1 < n && pos % p.block_size == 0) {
@@ -229,7 +239,7 @@ __global__ void __launch_bounds__(kCommitThreads)
 // order as in gdn_commit_kernel, and every chunk is read before any chunk of
 // the tile is written, so a boundary or final slot equal to the source is
 // still safe.
-template <int K, typename ST, int M, int G>
+template <int K, typename ST, int M, int G, bool KDA>
 __global__ void __launch_bounds__(kCommitThreads)
     gdn_commit_staged_kernel(const CommitParams p, int tiles_log2) {
   using C = Chunk<ST>;
@@ -258,17 +268,21 @@ __global__ void __launch_bounds__(kCommitThreads)
 
   float* u_s = smem;                     // [W][TILE_ROWS]
   float* k_s = u_s + p.W * TILE_ROWS;    // [W][K]
-  float* g_s = k_s + p.W * K;            // [W]
-  ST* tile_s = reinterpret_cast<ST*>(g_s + ((p.W + 3) & ~3));  // [rows][K], 16-byte aligned
+  float* g_s = k_s + p.W * K;            // [W], or [W][K] for the per-channel gate
+  ST* tile_s = reinterpret_cast<ST*>(g_s + ((p.W * (KDA ? K : 1) + 3) & ~3));  // [rows][K], 16-byte aligned
   const size_t rec = ((size_t)r * p.HV + h) * p.W;
   const float* ru = p.rec_u[layer] + rec * p.V + row_base;
   const float* rk = p.rec_k[layer] + rec * K;
-  const float* rg = p.rec_g[layer] + rec;
+  const float* rg = p.rec_g[layer] + rec * (KDA ? K : 1);
   const int urow4 = rows / 4;
   for (int i = tid; i < n * urow4; i += NT)
     cp_async16(u_s + (i / urow4) * TILE_ROWS + 4 * (i % urow4), ru + (size_t)(i / urow4) * p.V + 4 * (i % urow4));
   for (int i = tid; i < n * (K / 4); i += NT) cp_async16(k_s + 4 * i, rk + 4 * i);
-  if (tid < n) cp_async4(g_s + tid, rg + tid);
+  if constexpr (KDA) {
+    for (int i = tid; i < n * (K / 4); i += NT) cp_async16(g_s + 4 * i, rg + 4 * i);
+  } else {
+    if (tid < n) cp_async4(g_s + tid, rg + tid);
+  }
   const size_t head = (size_t)p.V * K;
   ST* pool = static_cast<ST*>(p.pools[layer]);
   const ST* S0 = pool + ((size_t)plan.src * p.HV + h) * head + (size_t)row_base * K;
@@ -293,7 +307,7 @@ __global__ void __launch_bounds__(kCommitThreads)
       if (c < nchunks) C::load_shared(tile_s + (size_t)(c - row_base * CPR) * E, x[m]);
     }
     for (int t = 0; t < n; ++t) {
-      fold_token<K, ST, G, NT>(x, g_s[t], k_s, u_s, t, TILE_ROWS, col, cg, row_base, nchunks);
+      fold_token<K, ST, G, NT, KDA>(x, g_s, k_s, u_s, t, TILE_ROWS, col, cg, row_base, nchunks);
       const long long pos = plan.p0 + t + 1;
       if (p.block_size > 0 && t + 1 < n && pos % p.block_size == 0) {
         const int bs = slot_after(trow, p.table_stride, p.block_size, pos);
@@ -305,7 +319,7 @@ __global__ void __launch_bounds__(kCommitThreads)
 }
 
 // --------------------------------------------------------------- launchers
-template <int K, typename ST, int M>
+template <int K, typename ST, int M, bool KDA>
 static int launch_commit_tiled_k(const CommitParams& p, cudaStream_t stream) {
   constexpr int CPR = K / Chunk<ST>::E;
   constexpr int TILE_ROWS = kCommitThreads * M / CPR;
@@ -313,8 +327,12 @@ static int launch_commit_tiled_k(const CommitParams& p, cudaStream_t stream) {
   int tiles_log2 = 0;
   while ((1 << tiles_log2) < tiles) ++tiles_log2;
   dim3 grid((unsigned)(p.HV << tiles_log2), p.batch, p.num_layers);
-  const size_t smem = sizeof(float) * ((size_t)p.W * (TILE_ROWS + K) + p.W);
-  gdn_commit_kernel<K, ST, M><<<grid, kCommitThreads, smem, stream>>>(p, tiles_log2);
+  const size_t smem = sizeof(float) * ((size_t)p.W * (TILE_ROWS + K) + (size_t)p.W * (KDA ? K : 1));
+  auto kern = gdn_commit_kernel<K, ST, M, KDA>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  kern<<<grid, kCommitThreads, smem, stream>>>(p, tiles_log2);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -322,18 +340,18 @@ static int launch_commit_tiled_k(const CommitParams& p, cudaStream_t stream) {
 // head): four such CTAs fit on an SM, and measured against whole-head and
 // 32-row tiles, and against a persistent kernel streaming heads through
 // shared memory with bulk asynchronous copies, it moves the most bytes.
-template <int K, typename ST>
+template <int K, typename ST, bool KDA>
 static int launch_commit_k(const CommitParams& p, cudaStream_t stream) {
   constexpr int CPR = K / Chunk<ST>::E;
   constexpr int MMAX = (128 * K) / Chunk<ST>::E / kCommitThreads;
   constexpr int MFULL = MMAX > 0 ? MMAX : 1;
   constexpr int M64 = (64 * CPR) / kCommitThreads;
   constexpr int M = M64 < 1 ? 1 : (M64 > MFULL ? MFULL : M64);
-  return launch_commit_tiled_k<K, ST, M>(p, stream);
+  return launch_commit_tiled_k<K, ST, M, KDA>(p, stream);
 }
 
 // bf16 states: whole 128-row heads staged in shared memory (see above).
-template <int K>
+template <int K, bool KDA>
 static int launch_commit_bf16_k(const CommitParams& p, cudaStream_t stream) {
   using ST = __nv_bfloat16;
   constexpr int CPR = K / Chunk<ST>::E;
@@ -344,9 +362,10 @@ static int launch_commit_bf16_k(const CommitParams& p, cudaStream_t stream) {
   int tiles_log2 = 0;
   while ((1 << tiles_log2) < tiles) ++tiles_log2;
   dim3 grid((unsigned)(p.HV << tiles_log2), p.batch, p.num_layers);
-  const size_t smem = sizeof(float) * ((size_t)p.W * (TILE_ROWS + K) + ((p.W + 3) & ~3)) +
+  const size_t smem = sizeof(float) * ((size_t)p.W * (TILE_ROWS + K) +
+                                       (((size_t)p.W * (KDA ? K : 1) + 3) & ~(size_t)3)) +
                       (size_t)TILE_ROWS * K * sizeof(ST);
-  auto kern = gdn_commit_staged_kernel<K, ST, M, G>;
+  auto kern = gdn_commit_staged_kernel<K, ST, M, G, KDA>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return GDN_ERR_CUDA;
@@ -354,13 +373,24 @@ static int launch_commit_bf16_k(const CommitParams& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-int launch_commit(const CommitParams& p, int head_k, int state_dtype, cudaStream_t stream) {
+template <int K, bool KDA>
+static int launch_commit_dtype(const CommitParams& p, bool bf, cudaStream_t stream) {
+  return bf ? launch_commit_bf16_k<K, KDA>(p, stream) : launch_commit_k<K, float, KDA>(p, stream);
+}
+
+int launch_commit(const CommitParams& p, int head_k, int state_dtype, bool kda,
+                  cudaStream_t stream) {
   const bool bf = state_dtype == GDN_DTYPE_BF16;
   switch (head_k) {
-    case 16: return bf ? launch_commit_bf16_k<16>(p, stream) : launch_commit_k<16, float>(p, stream);
-    case 32: return bf ? launch_commit_bf16_k<32>(p, stream) : launch_commit_k<32, float>(p, stream);
-    case 64: return bf ? launch_commit_bf16_k<64>(p, stream) : launch_commit_k<64, float>(p, stream);
-    case 128: return bf ? launch_commit_bf16_k<128>(p, stream) : launch_commit_k<128, float>(p, stream);
+#define GDN_CASE(KK)                                                                  \
+  case KK:                                                                            \
+    return kda ? launch_commit_dtype<KK, true>(p, bf, stream)                         \
+               : launch_commit_dtype<KK, false>(p, bf, stream);
+    GDN_CASE(16)
+    GDN_CASE(32)
+    GDN_CASE(64)
+    GDN_CASE(128)
+#undef GDN_CASE
     default: return GDN_ERR_UNSUPPORTED;
   }
 }

@@ -58,24 +58,26 @@ struct VerifyTile {
   static constexpr int VT = WARPS * RPW * RPT;    // state rows per tile
   // CTAs per SM the registers must allow, as measured: seven (72 registers)
   // for the native form and for the verify with a bf16 state; six (80
-  // registers) for the verify with an fp32 state, which spills at 72.
-  template <bool NATIVE, typename ST>
+  // registers) for the verify with an fp32 state, which spills at 72.  The
+  // per-channel (KDA) gate holds eight more pairs per thread: five (96).
+  template <bool NATIVE, typename ST, bool KDA>
   static constexpr int min_ctas() {
-    return (!NATIVE && sizeof(ST) == 4) ? 6 : 7;
+    return KDA ? 5 : ((!NATIVE && sizeof(ST) == 4) ? 6 : 7);
   }
 };
 
 // Dynamic shared memory of one verify CTA covering NS tiles, in bytes: the
 // mbarrier (16 bytes), the tile buffer the bulk copies fill (NS > 1 only),
-// then the staged keys, queries, values and gates.
+// then the staged keys, queries, values and gates (plus, for the
+// per-channel KDA gate, the window's [W][K] decay vectors).
 template <int K, typename ST>
 __host__ __device__ constexpr size_t verify_tile_bytes(int NS) {
   return NS > 1 ? (size_t)VerifyTile<K>::VT * K * sizeof(ST) : 0;
 }
-template <int K, typename ST>
+template <int K, typename ST, bool KDA>
 __host__ __device__ constexpr size_t verify_smem_bytes(int W, int NS) {
   return 16 + verify_tile_bytes<K, ST>(NS) +
-         sizeof(float) * (size_t)W * (2 * K + NS * VerifyTile<K>::VT + 4);
+         sizeof(float) * (size_t)W * (2 * K + NS * VerifyTile<K>::VT + 4 + (KDA ? K : 0));
 }
 
 // A tile's checkpoint rows from the shared-memory tile buffer (a verbatim
@@ -131,12 +133,14 @@ __device__ __forceinline__ void load_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], con
 }
 
 // The draft window over one tile whose state is in s.  vt_off: this tile's
-// first row inside the CTA's staged value rows.
-template <int K, typename ST, bool NATIVE, bool FULL>
+// first row inside the CTA's staged value rows.  al_s: the window's
+// per-channel decay vectors [W][K] (KDA), unused for the scalar gate.
+template <int K, typename ST, bool NATIVE, bool FULL, bool KDA>
 __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], const VerifyParams& p,
                                          int tile, int h, int r, int w, long long t0, int vt_off,
                                          int vrow_stride, const float* kh_s, const float* qh_s,
-                                         const float* v_s, const float* gs_s, int warp, int l, int lr) {
+                                         const float* v_s, const float* gs_s, const float* al_s,
+                                         int warp, int l, int lr) {
   using Tile = VerifyTile<K>;
   constexpr int LPR = Tile::LPR, RPW = Tile::RPW, RPT = Tile::RPT, VT = Tile::VT;
   const size_t rec_base = ((size_t)r * p.HV + h) * p.W;
@@ -168,19 +172,24 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
     const f32x2 al2 = gq.x;  // (alpha, alpha)
     const float2 bk = unpack2(gq.y);
     const float be = bk.x, kq = bk.y;
-    f32x2 kk[8], qq[8];
+    f32x2 kk[8], qq[8], aa[KDA ? 8 : 1];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kh_s + t * K + 4 * (l + LPR * m));
       const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(qh_s + t * K + 4 * (l + LPR * m));
       kk[2 * m] = k4.x; kk[2 * m + 1] = k4.y;
       qq[2 * m] = q4.x; qq[2 * m + 1] = q4.y;
+      if constexpr (KDA) {
+        // the decay of this thread's own columns: S diag(alpha)
+        const ulonglong2 a4 = *reinterpret_cast<const ulonglong2*>(al_s + t * K + 4 * (l + LPR * m));
+        aa[2 * m] = a4.x; aa[2 * m + 1] = a4.y;
+      }
     }
 #pragma unroll
     for (int g = 0; g < RPT; ++g) {
       // H = alpha * S
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], al2);
+      for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], KDA ? aa[KDA ? j : 0] : al2);
       // d = H khat and H qhat in one pass: pair accumulators over pairs
       // 0-3 and 4-7, combined pairwise, lanes summed, then the LPR lanes
       f32x2 da = mul2(s[g][0], kk[0]), db = mul2(s[g][4], kk[4]);
@@ -240,9 +249,9 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
 // One CTA runs NS consecutive tiles of one (request row, value head): the
 // window's keys, queries, gates and values are staged once for all of them,
 // then each tile's checkpoint rows are loaded and its window run in turn.
-template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS>
+template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS, bool KDA>
 __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
-                                  VerifyTile<K>::template min_ctas<NATIVE, ST>())
+                                  VerifyTile<K>::template min_ctas<NATIVE, ST, KDA>())
     gdn_verify_kernel(const VerifyParams p) {
   using Tile = VerifyTile<K>;
   constexpr int LPR = Tile::LPR, RPT = Tile::RPT, VT = Tile::VT;
@@ -269,7 +278,8 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   if (src.err) {
     if (p.err && tid == 0 && span == 0 && h == 0) atomicOr(p.err, src.err);
     // the reject marker tells the commit not to fold this row's stale record
-    if (!NATIVE && tid == 0 && span == 0) p.rec_g[((size_t)r * p.HV + h) * p.W] = kRejectedGate;
+    if (!NATIVE && tid == 0 && span == 0)
+      p.rec_g[((size_t)r * p.HV + h) * p.W * (KDA ? K : 1)] = kRejectedGate;
     return;
   }
   if (src.slot < 0) return;  // null row or empty window: writes nothing
@@ -304,6 +314,7 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   float* qh_s = kh_s + p.W * K;         // [W][K]
   float* v_s = qh_s + p.W * K;          // [W][SV]
   float* gs_s = v_s + p.W * SV;         // [W][4]: alpha, alpha, beta, khat . qhat
+  float* al_s = gs_s + 4 * p.W;         // [W][K]: per-channel decay (KDA only)
   const QKV* qb = static_cast<const QKV*>(p.q);
   const QKV* kb = static_cast<const QKV*>(p.k);
   const QKV* vb = static_cast<const QKV*>(p.v);
@@ -345,13 +356,24 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
     }
     if (lane == 0) gs_s[4 * t + 3] = kq;
   }
-  // gates of the whole window: one lane per token in the last warp
+  // gates of the whole window: one lane per token in the last warp; the
+  // per-channel decay (KDA) one element per thread: a [T][HV][K],
+  // dt_bias [HV][K]
   if (warp == Tile::WARPS - 1 && lane < w) {
     const size_t gi = (size_t)(t0 + lane) * p.HV + h;
-    const float al = gate_decay(p.a[gi], p.A_log[h], p.dt_bias[h]);
-    gs_s[4 * lane] = al;
-    gs_s[4 * lane + 1] = al;
+    if constexpr (!KDA) {
+      const float al = gate_decay(p.a[gi], p.A_log[h], p.dt_bias[h]);
+      gs_s[4 * lane] = al;
+      gs_s[4 * lane + 1] = al;
+    }
     gs_s[4 * lane + 2] = gate_beta(p.b[gi]);
+  }
+  if constexpr (KDA) {
+    const float A = p.A_log[h];
+    for (int i = tid; i < w * K; i += Tile::THREADS) {
+      const int t = i / K, j = i % K;
+      al_s[i] = gate_decay(p.a[((size_t)(t0 + t) * p.HV + h) * K + j], A, p.dt_bias[(size_t)h * K + j]);
+    }
   }
   // the value rows of this CTA's tiles, every token, all threads
   for (int i = tid; i < w * SV; i += Tile::THREADS) {
@@ -363,7 +385,11 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   const size_t rec_base = ((size_t)r * p.HV + h) * p.W;  // record position 0
   if (!NATIVE && span == 0) {
     for (int i = tid; i < w * K; i += Tile::THREADS) p.rec_k[rec_base * K + i] = kh_s[i];
-    if (tid < w) p.rec_g[rec_base + tid] = gs_s[4 * tid];
+    if constexpr (KDA) {
+      for (int i = tid; i < w * K; i += Tile::THREADS) p.rec_g[rec_base * K + i] = al_s[i];
+    } else {
+      if (tid < w) p.rec_g[rec_base + tid] = gs_s[4 * tid];
+    }
   }
 
   // ---- the tiles one after another.  With bulk copies, tile i + 1 is
@@ -388,17 +414,17 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
     } else {
       if (i > 0) load_tile<K, ST, FULL>(s, S0, tile0 + i, p.V, warp, l, lr);
     }
-    run_tile<K, ST, NATIVE, FULL>(s, p, tile0 + i, h, r, w, t0, i * VT, SV, kh_s, qh_s, v_s, gs_s,
-                                  warp, l, lr);
+    run_tile<K, ST, NATIVE, FULL, KDA>(s, p, tile0 + i, h, r, w, t0, i * VT, SV, kh_s, qh_s, v_s,
+                                       gs_s, al_s, warp, l, lr);
   }
 }
 
-template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS>
+template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS, bool KDA>
 static void launch_tiles(const VerifyParams& p, int ntiles, cudaStream_t stream) {
   using Tile = VerifyTile<K>;
   dim3 grid(ntiles / NS, p.HV, p.batch);
-  const size_t smem = verify_smem_bytes<K, ST>(p.W, NS);
-  auto kern = gdn_verify_kernel<K, QKV, ST, NATIVE, FULL, NS>;
+  const size_t smem = verify_smem_bytes<K, ST, KDA>(p.W, NS);
+  auto kern = gdn_verify_kernel<K, QKV, ST, NATIVE, FULL, NS, KDA>;
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   kern<<<grid, Tile::THREADS, smem, stream>>>(p);
@@ -406,7 +432,7 @@ static void launch_tiles(const VerifyParams& p, int ntiles, cudaStream_t stream)
 
 // The verify runs 4 (else 2) tiles of a head per CTA when they divide the
 // head; the native baseline, and heads smaller than a tile, one per CTA.
-template <int K, typename QKV, typename ST, bool NATIVE>
+template <int K, typename QKV, typename ST, bool NATIVE, bool KDA>
 static int launch_one(const VerifyParams& p, cudaStream_t stream) {
   using Tile = VerifyTile<K>;
   const int ntiles = (p.V + Tile::VT - 1) / Tile::VT;
@@ -414,46 +440,50 @@ static int launch_one(const VerifyParams& p, cudaStream_t stream) {
   bool done = false;
   if constexpr (!NATIVE) {
     if (full && ntiles % 4 == 0) {
-      launch_tiles<K, QKV, ST, NATIVE, true, 4>(p, ntiles, stream);
+      launch_tiles<K, QKV, ST, NATIVE, true, 4, KDA>(p, ntiles, stream);
       done = true;
     } else if (full && ntiles % 2 == 0) {
-      launch_tiles<K, QKV, ST, NATIVE, true, 2>(p, ntiles, stream);
+      launch_tiles<K, QKV, ST, NATIVE, true, 2, KDA>(p, ntiles, stream);
       done = true;
     }
   }
   if (!done) {
-    if (full) launch_tiles<K, QKV, ST, NATIVE, true, 1>(p, ntiles, stream);
-    else launch_tiles<K, QKV, ST, NATIVE, false, 1>(p, ntiles, stream);
+    if (full) launch_tiles<K, QKV, ST, NATIVE, true, 1, KDA>(p, ntiles, stream);
+    else launch_tiles<K, QKV, ST, NATIVE, false, 1, KDA>(p, ntiles, stream);
   }
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-template <int K, bool NATIVE>
+template <int K, bool NATIVE, bool KDA>
 static int dispatch_dtypes(const VerifyParams& p, int qkv_dtype, int state_dtype,
                            cudaStream_t stream) {
   if (qkv_dtype == GDN_DTYPE_F32 && state_dtype == GDN_DTYPE_F32)
-    return launch_one<K, float, float, NATIVE>(p, stream);
+    return launch_one<K, float, float, NATIVE, KDA>(p, stream);
   if (qkv_dtype == GDN_DTYPE_F32 && state_dtype == GDN_DTYPE_BF16)
-    return launch_one<K, float, __nv_bfloat16, NATIVE>(p, stream);
+    return launch_one<K, float, __nv_bfloat16, NATIVE, KDA>(p, stream);
   if (qkv_dtype == GDN_DTYPE_BF16 && state_dtype == GDN_DTYPE_F32)
-    return launch_one<K, __nv_bfloat16, float, NATIVE>(p, stream);
-  return launch_one<K, __nv_bfloat16, __nv_bfloat16, NATIVE>(p, stream);
+    return launch_one<K, __nv_bfloat16, float, NATIVE, KDA>(p, stream);
+  return launch_one<K, __nv_bfloat16, __nv_bfloat16, NATIVE, KDA>(p, stream);
+}
+
+template <int K>
+static int dispatch_modes(const VerifyParams& p, int qkv_dtype, int state_dtype, bool native,
+                          bool kda, cudaStream_t stream) {
+  if (kda)
+    return native ? dispatch_dtypes<K, true, true>(p, qkv_dtype, state_dtype, stream)
+                  : dispatch_dtypes<K, false, true>(p, qkv_dtype, state_dtype, stream);
+  return native ? dispatch_dtypes<K, true, false>(p, qkv_dtype, state_dtype, stream)
+                : dispatch_dtypes<K, false, false>(p, qkv_dtype, state_dtype, stream);
 }
 
 int launch_verify(const VerifyParams& p, int head_k, int qkv_dtype, int state_dtype,
-                  bool native, cudaStream_t stream) {
+                  bool native, bool kda, cudaStream_t stream) {
   switch (head_k) {
-#define GDN_CASE(KK)                                                              \
-  case KK:                                                                        \
-    return native ? dispatch_dtypes<KK, true>(p, qkv_dtype, state_dtype, stream)  \
-                  : dispatch_dtypes<KK, false>(p, qkv_dtype, state_dtype, stream);
-    GDN_CASE(16)
-    GDN_CASE(32)
-    GDN_CASE(64)
-    GDN_CASE(128)
-#undef GDN_CASE
-    default:
-      return GDN_ERR_UNSUPPORTED;
+    case 16: return dispatch_modes<16>(p, qkv_dtype, state_dtype, native, kda, stream);
+    case 32: return dispatch_modes<32>(p, qkv_dtype, state_dtype, native, kda, stream);
+    case 64: return dispatch_modes<64>(p, qkv_dtype, state_dtype, native, kda, stream);
+    case 128: return dispatch_modes<128>(p, qkv_dtype, state_dtype, native, kda, stream);
+    default: return GDN_ERR_UNSUPPORTED;
   }
 }
 

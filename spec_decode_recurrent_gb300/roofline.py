@@ -2,11 +2,12 @@
 bytes, not the traffic of any particular implementation).
 
 Per live (layer, row r, value head) unit, with e = state element bytes,
-q = q/k/v element bytes, w = window_len[r], n = accepted_len[r]:
-  commit   V*K*e read + (1 + boundaries) * V*K*e written + n*(V+K+1)*4 record read
-  verify   V*K*e read + w*(V*4 out + (V+K+1)*4 record + V*q value + 8 gates)
+q = q/k/v element bytes, w = window_len[r], n = accepted_len[r] and G the
+gate width (1 for the scalar decay, K for the per-channel KDA decay):
+  commit   V*K*e read + (1 + boundaries) * V*K*e written + n*(V+K+G)*4 record read
+  verify   V*K*e read + w*(V*4 out + (V+K+G)*4 record + V*q value + 4*G + 4 gates)
            plus, per (row, key head), w*2*K*q for q and k
-  native   V*K*e read + w*V*K*e snapshots + w*(V*4 out + V*q value + 8 gates)
+  native   V*K*e read + w*V*K*e snapshots + w*(V*4 out + V*q value + 4*G + 4 gates)
            plus the same q and k bytes
 Rows with a null slot, an empty window or n = 0 move no bytes.
 """
@@ -37,9 +38,13 @@ def state_bytes(sb: SpecBatch) -> int:
     return sb.V * sb.K * (2 if sb.state_dtype.itemsize == 2 else 4)
 
 
+def gate_width(sb: SpecBatch) -> int:
+    return sb.K if getattr(sb, "kda", False) else 1
+
+
 def commit_bytes(sb: SpecBatch) -> int:
     S = state_bytes(sb)
-    rec = (sb.V + sb.K + 1) * 4
+    rec = (sb.V + sb.K + gate_width(sb)) * 4
     total = 0
     for r, w, n, p0 in _rows(sb):
         if n <= 0:
@@ -54,7 +59,8 @@ def commit_bytes(sb: SpecBatch) -> int:
 def verify_bytes_per_layer(sb: SpecBatch) -> int:
     S = state_bytes(sb)
     qb = sb.qkv_dtype.itemsize
-    per_tok = sb.V * 4 + (sb.V + sb.K + 1) * 4 + sb.V * qb + 8
+    G = gate_width(sb)
+    per_tok = sb.V * 4 + (sb.V + sb.K + G) * 4 + sb.V * qb + 4 * G + 4
     total = 0
     for r, w, n, p0 in _rows(sb):
         total += sb.HV * (S + w * per_tok) + sb.HK * w * 2 * sb.K * qb
@@ -64,7 +70,7 @@ def verify_bytes_per_layer(sb: SpecBatch) -> int:
 def native_bytes_per_layer(sb: SpecBatch) -> int:
     S = state_bytes(sb)
     qb = sb.qkv_dtype.itemsize
-    per_tok = S + sb.V * 4 + sb.V * qb + 8
+    per_tok = S + sb.V * 4 + sb.V * qb + 4 * gate_width(sb) + 4
     total = 0
     for r, w, n, p0 in _rows(sb):
         total += sb.HV * (S + w * per_tok) + sb.HK * w * 2 * sb.K * qb

@@ -26,13 +26,15 @@ class StepBuffers:
         self.out = list(self.out_all.unbind(0))
         self.rec_u = [make((sb.B, sb.HV, sb.W, sb.V)) for _ in range(sb.L)]
         self.rec_k = [make((sb.B, sb.HV, sb.W, sb.K)) for _ in range(sb.L)]
-        self.rec_g = [make((sb.B, sb.HV, sb.W)) for _ in range(sb.L)]
+        gshape = (sb.B, sb.HV, sb.W, sb.K) if sb.kda else (sb.B, sb.HV, sb.W)
+        self.rec_g = [make(gshape) for _ in range(sb.L)]
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.table = api.LayerTable(sb.pools, self.rec_u, self.rec_k, self.rec_g)
 
 
 def verify_layer(sb: SpecBatch, bufs: StepBuffers, layer: int, stream=None) -> None:
-    api.gdn_spec_verify(
+    fn = api.gdn_kda_spec_verify if sb.kda else api.gdn_spec_verify
+    fn(
         q=sb.q[layer], k=sb.k[layer], v=sb.v[layer], a=sb.a[layer], b=sb.b[layer],
         A_log=sb.A_log[layer], dt_bias=sb.dt_bias[layer], token_start=sb.token_start,
         window_len=sb.window_len, state_pool=sb.pools[layer], slot_table=sb.slot_table,
@@ -55,7 +57,8 @@ def commit(sb: SpecBatch, bufs: StepBuffers, stream=None) -> None:
 
 def native_layer(sb: SpecBatch, layer: int, out: torch.Tensor, snapshots: torch.Tensor,
                  err: Optional[torch.Tensor] = None, stream=None) -> None:
-    api.gdn_native_spec_snapshot(
+    fn = api.gdn_kda_native_spec_snapshot if sb.kda else api.gdn_native_spec_snapshot
+    fn(
         q=sb.q[layer], k=sb.k[layer], v=sb.v[layer], a=sb.a[layer], b=sb.b[layer],
         A_log=sb.A_log[layer], dt_bias=sb.dt_bias[layer], token_start=sb.token_start,
         window_len=sb.window_len, state_pool=sb.pools[layer], slot_table=sb.slot_table,

@@ -20,6 +20,7 @@ Named workloads (sizes are those of the five benchmark configurations):
                 non-contiguous strided rows, extreme gates, three seeds
   align         36 layers, batch 128, window 4, block size 4, align mode,
                 fp32 or bf16 state
+  kda_all_layer the all_layer shapes with a per-channel (KDA) decay
 """
 from __future__ import annotations
 
@@ -70,6 +71,7 @@ class SpecBatch:
     slot_table: torch.Tensor
     seq_pos: Optional[torch.Tensor]
     fused_qkv: Optional[List[torch.Tensor]] = None
+    kda: bool = False     # per-channel decay: a [T, HV, K], dt_bias [HV, K]
 
     @property
     def device(self) -> torch.device:
@@ -91,7 +93,7 @@ def _uniform(shape, lo, hi, gen, device):
 
 def _make(name, *, HK, HV, K, V, W, L, windows, accepted, num_slots, slots_for_row,
           seq_pos=None, block_size=0, qkv_dtype, state_dtype, gen, device,
-          sentinel, gate_range=None, gaps=None, row_order=None, fused=False):
+          sentinel, gate_range=None, gaps=None, row_order=None, fused=False, kda=False):
     """Lay out one step and draw its tensors.
 
     windows/accepted: per-row lists.  slots_for_row: list of per-row tables
@@ -138,14 +140,15 @@ def _make(name, *, HK, HV, K, V, W, L, windows, accepted, num_slots, slots_for_r
             q.append(torch.randn((T, HK, K), generator=gen, device=device, dtype=F32).to(qkv_dtype))
             k.append(torch.randn((T, HK, K), generator=gen, device=device, dtype=F32).to(qkv_dtype))
             v.append(torch.randn((T, HV, V), generator=gen, device=device, dtype=F32).to(qkv_dtype))
+        ga = (T, HV, K) if kda else (T, HV)       # per-channel gate inputs for KDA
         if gate_range is None:
-            a.append(torch.randn((T, HV), generator=gen, device=device, dtype=F32))
+            a.append(torch.randn(ga, generator=gen, device=device, dtype=F32))
             b.append(torch.randn((T, HV), generator=gen, device=device, dtype=F32))
         else:
-            a.append(_uniform((T, HV), -gate_range, gate_range, gen, device))
+            a.append(_uniform(ga, -gate_range, gate_range, gen, device))
             b.append(_uniform((T, HV), -gate_range, gate_range, gen, device))
         A_log.append(_uniform((HV,), 0.0, math.log(16.0), gen, device))
-        dt_bias.append(_uniform((HV,), -1.0, 1.0, gen, device))
+        dt_bias.append(_uniform((HV, K) if kda else (HV,), -1.0, 1.0, gen, device))
         state = (torch.randn((num_slots, HV, V, K), generator=gen, device=device, dtype=F32)
                  * 0.1).to(state_dtype)
         if sentinel:
@@ -165,7 +168,7 @@ def _make(name, *, HK, HV, K, V, W, L, windows, accepted, num_slots, slots_for_r
         token_start=as_i32(token_start), window_len=as_i32(list(windows)),
         accepted_len=as_i32(list(accepted)), slot_table=table.to(dev),
         seq_pos=None if seq_pos is None else as_i32(list(seq_pos)),
-        fused_qkv=fused_list if fused else None)
+        fused_qkv=fused_list if fused else None, kda=kda)
 
 
 def _gen(seed, device):
@@ -203,7 +206,7 @@ def layer(device="cpu", sentinel=True, seed=1, batch=16, HK=16, HV=32, KV=128, L
 
 
 def all_layer(device="cpu", sentinel=True, seed=2, L=36, batch=64, pad_rows=8, HK=16, HV=32,
-              KV=128, num_slots=256, window=4, state_dtype=F32):
+              KV=128, num_slots=256, window=4, state_dtype=F32, kda=False):
     """All-layer commit workload: live rows then graph-padding rows (slot -1, window 0)."""
     cpu = _gen(seed, "cpu")
     live = batch - pad_rows
@@ -212,10 +215,17 @@ def all_layer(device="cpu", sentinel=True, seed=2, L=36, batch=64, pad_rows=8, H
     perm = torch.randperm(num_slots, generator=cpu).tolist()
     slots = [[perm[r]] for r in range(live)] + [[-1]] * pad_rows
     gen = _gen(seed, device)
-    return _make("all_layer", HK=HK, HV=HV, K=KV, V=KV, W=window, L=L, windows=windows,
-                 accepted=accepted, num_slots=num_slots, slots_for_row=slots,
-                 qkv_dtype=BF16, state_dtype=state_dtype, gen=gen, device=device,
-                 sentinel=sentinel)
+    return _make("kda_all_layer" if kda else "all_layer", HK=HK, HV=HV, K=KV, V=KV, W=window,
+                 L=L, windows=windows, accepted=accepted, num_slots=num_slots,
+                 slots_for_row=slots, qkv_dtype=BF16, state_dtype=state_dtype, gen=gen,
+                 device=device, sentinel=sentinel, kda=kda)
+
+
+def kda_all_layer(device="cpu", sentinel=True, seed=6, state_dtype=F32, **kw):
+    """The all_layer shapes with the per-channel (KDA) decay: gate inputs
+    a [T, HV, K] ~ N(0, 1) and dt_bias [HV, K] ~ U(-1, 1)."""
+    return all_layer(device=device, sentinel=sentinel, seed=seed, state_dtype=state_dtype,
+                     kda=True, **kw)
 
 
 # Per-position acceptance rates of a five-draft (window 6) run, P(n >= 1 + i)
@@ -314,12 +324,14 @@ WORKLOADS = {
     "mtp5": mtp5,
     "long_ragged": long_ragged,
     "align": align,
+    "kda_all_layer": kda_all_layer,
 }
 
 
 def custom(device="cpu", sentinel=True, seed=100, *, HK, HV, K, V, W, L, windows, accepted,
            null_rows=(), num_slots=None, block_size=0, seq_pos=None, qkv_dtype=F32,
-           state_dtype=F32, gate_range=None, gaps=None, shuffle_rows=False, fused=False):
+           state_dtype=F32, gate_range=None, gaps=None, shuffle_rows=False, fused=False,
+           kda=False):
     """A small step with explicit per-row windows / accepted lengths, for
     parity cases the oracle runs in full.  Rows listed in null_rows get the
     null slot.  In align mode (block_size > 0) seq_pos must be given and each
@@ -352,7 +364,7 @@ def custom(device="cpu", sentinel=True, seed=100, *, HK, HV, K, V, W, L, windows
                  accepted=list(accepted), num_slots=num_slots, slots_for_row=tables,
                  seq_pos=seq_pos, block_size=block_size, qkv_dtype=qkv_dtype,
                  state_dtype=state_dtype, gen=gen, device=device, sentinel=sentinel,
-                 gate_range=gate_range, gaps=gaps, row_order=order, fused=fused)
+                 gate_range=gate_range, gaps=gaps, row_order=order, fused=fused, kda=kda)
 
 
 def conv_state(sb: SpecBatch, state_len: int = 3, dtype=BF16, seed: int = 200):

@@ -145,9 +145,16 @@ class GpuStep:
         src, writes = self.plans[r]
         S0 = cpu64(self.before[l][src, h])
         sl = slice(t0, t0 + w)
-        ref = oracle.window(S0, cpu64(sb.q[l][sl, hk]), cpu64(sb.k[l][sl, hk]),
-                            cpu64(sb.v[l][sl, h]), cpu64(sb.a[l][sl, h]), cpu64(sb.b[l][sl, h]),
-                            float(sb.A_log[l][h]), float(sb.dt_bias[l][h]))
+        if sb.kda:
+            ref = oracle.kda_window(S0, cpu64(sb.q[l][sl, hk]), cpu64(sb.k[l][sl, hk]),
+                                    cpu64(sb.v[l][sl, h]), cpu64(sb.a[l][sl, h]),
+                                    cpu64(sb.b[l][sl, h]), float(sb.A_log[l][h]),
+                                    cpu64(sb.dt_bias[l][h]))
+        else:
+            ref = oracle.window(S0, cpu64(sb.q[l][sl, hk]), cpu64(sb.k[l][sl, hk]),
+                                cpu64(sb.v[l][sl, h]), cpu64(sb.a[l][sl, h]),
+                                cpu64(sb.b[l][sl, h]), float(sb.A_log[l][h]),
+                                float(sb.dt_bias[l][h]))
         tag = f"layer {l} row {r} head {h}"
         check_close(cpu64(self.bufs.out[l][sl, h]), ref["o"], f"{tag}: out")
         check_close(cpu64(self.bufs.rec_u[l][r, h, :w]), ref["u"], f"{tag}: record u")
@@ -169,13 +176,15 @@ def oracle_full(sb, pools_before):
     the all-layer commit from the oracle's own records."""
     sp = None if sb.seq_pos is None else sb.seq_pos.cpu()
     layers = []
+    verify = oracle.kda_spec_verify if sb.kda else oracle.spec_verify
     for l in range(sb.L):
-        layers.append(oracle.spec_verify(
+        layers.append(verify(
             q=sb.q[l].cpu(), k=sb.k[l].cpu(), v=sb.v[l].cpu(), a=sb.a[l].cpu(), b=sb.b[l].cpu(),
             A_log=sb.A_log[l].cpu(), dt_bias=sb.dt_bias[l].cpu(), token_start=sb.token_start.cpu(),
             window_len=sb.window_len.cpu(), pool=pools_before[l].cpu(), slot_table=sb.slot_table.cpu(),
             seq_pos=sp, block_size=sb.block_size, max_window=sb.W, snapshots=True))
-    pools, err = oracle.replay_commit(
+    commit = oracle.kda_replay_commit if sb.kda else oracle.replay_commit
+    pools, err = commit(
         pools=np.stack([cpu64(p) for p in pools_before]),
         rec_u=np.stack([x["rec_u"] for x in layers]), rec_k=np.stack([x["rec_k"] for x in layers]),
         rec_g=np.stack([x["rec_g"] for x in layers]), window_len=sb.window_len.cpu(),
