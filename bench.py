@@ -243,7 +243,8 @@ COMMIT_SOURCES = ["spec_decode_recurrent_gb300/csrc/gdn_commit.cu",
                   "spec_decode_recurrent_gb300/csrc/gdn_device.cuh",
                   "spec_decode_recurrent_gb300/csrc/gdn_async.cuh"]
 VERIFY_SOURCES = ["spec_decode_recurrent_gb300/csrc/gdn_verify.cu",
-                  "spec_decode_recurrent_gb300/csrc/gdn_device.cuh"]
+                  "spec_decode_recurrent_gb300/csrc/gdn_device.cuh",
+                  "spec_decode_recurrent_gb300/csrc/gdn_async.cuh"]
 
 
 def profiled_traffic(kernel, workload, sources, state_dtype="f32"):

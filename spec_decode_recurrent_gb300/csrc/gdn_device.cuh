@@ -99,10 +99,15 @@ __device__ __forceinline__ float softplus(float x) {
   return x > 0.0f ? __fadd_rn(x, log1pf(expf(-x))) : log1pf(expf(x));
 }
 
+// Decay alpha = exp(g), g = -A * softplus(a + dt_bias), with A = exp(A_log)
+// evaluated once per head by the caller.
+__device__ __forceinline__ float gate_decay_scaled(float a, float A, float dt_bias) {
+  float g = -__fmul_rn(A, softplus(__fadd_rn(a, dt_bias)));
+  return expf(g);
+}
 // Decay alpha = exp(g), g = -exp(A_log) * softplus(a + dt_bias).
 __device__ __forceinline__ float gate_decay(float a, float A_log, float dt_bias) {
-  float g = -__fmul_rn(expf(A_log), softplus(__fadd_rn(a, dt_bias)));
-  return expf(g);
+  return gate_decay_scaled(a, expf(A_log), dt_bias);
 }
 
 // Write strength beta = sigmoid(b).

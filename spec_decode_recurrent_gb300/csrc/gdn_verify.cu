@@ -369,10 +369,11 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
     gs_s[4 * lane + 2] = gate_beta(p.b[gi]);
   }
   if constexpr (KDA) {
-    const float A = p.A_log[h];
+    const float A = expf(p.A_log[h]);  // once per head, not per channel
     for (int i = tid; i < w * K; i += Tile::THREADS) {
       const int t = i / K, j = i % K;
-      al_s[i] = gate_decay(p.a[((size_t)(t0 + t) * p.HV + h) * K + j], A, p.dt_bias[(size_t)h * K + j]);
+      al_s[i] = gate_decay_scaled(p.a[((size_t)(t0 + t) * p.HV + h) * K + j], A,
+                                  p.dt_bias[(size_t)h * K + j]);
     }
   }
   // the value rows of this CTA's tiles, every token, all threads
