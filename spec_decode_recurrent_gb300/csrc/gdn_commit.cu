@@ -91,14 +91,16 @@ struct Chunk<__nv_bfloat16> {
   static __device__ __forceinline__ void load_shared(const __nv_bfloat16* p, f32x2 (&y)[4]) {
     widen(*reinterpret_cast<const uint4*>(p), y);
   }
+  // Two fp32 values rounded to nearest even into one bf16 pair by a single
+  // packed conversion (the same rounding as two scalar conversions).
+  static __device__ __forceinline__ uint32_t round_pair(f32x2 v) {
+    const float2 f = unpack2(v);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y), "f"(f.x));  // high <- y, low <- x
+    return r;
+  }
   static __device__ __forceinline__ void store(__nv_bfloat16* p, const f32x2 (&y)[4]) {
-    uint4 t;
-    uint32_t* w = &t.x;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = unpack2(y[i]);
-      w[i] = pack_bf16x2(f.x, f.y);
-    }
+    const uint4 t = make_uint4(round_pair(y[0]), round_pair(y[1]), round_pair(y[2]), round_pair(y[3]));
     __stcs(reinterpret_cast<uint4*>(p), t);
   }
 };
@@ -239,8 +241,8 @@ __global__ void __launch_bounds__(kCommitThreads)
 // order as in gdn_commit_kernel, and every chunk is read before any chunk of
 // the tile is written, so a boundary or final slot equal to the source is
 // still safe.
-template <int K, typename ST, int M, int G, bool KDA>
-__global__ void __launch_bounds__(kCommitThreads)
+template <int K, typename ST, int M, int G, bool KDA, bool FULL>
+__global__ void __launch_bounds__(kCommitThreads, 4)
     gdn_commit_staged_kernel(const CommitParams p, int tiles_log2) {
   using C = Chunk<ST>;
   constexpr int E = C::E;
@@ -295,8 +297,11 @@ __global__ void __launch_bounds__(kCommitThreads)
     return;
   }
 
+  // FULL: the head is a whole number of tiles, so every chunk a thread
+  // names exists and no per-chunk guard is needed
   const int nchunks = (row_base + rows) * CPR;  // end of this tile's chunks in the head
   const int col = (tid % CPR) * E;
+  const size_t fin_off = ((size_t)plan.fin * p.HV + h) * head;
 #pragma unroll 1
   for (int grp = 0; grp < M / G; ++grp) {
     const int cg = row_base * CPR + tid + NT * G * grp;  // first chunk of this group (head index)
@@ -304,17 +309,41 @@ __global__ void __launch_bounds__(kCommitThreads)
 #pragma unroll
     for (int m = 0; m < G; ++m) {
       const int c = cg + NT * m;
-      if (c < nchunks) C::load_shared(tile_s + (size_t)(c - row_base * CPR) * E, x[m]);
+      if (FULL || c < nchunks) C::load_shared(tile_s + (size_t)(c - row_base * CPR) * E, x[m]);
     }
     for (int t = 0; t < n; ++t) {
-      fold_token<K, ST, G, NT, KDA>(x, g_s, k_s, u_s, t, TILE_ROWS, col, cg, row_base, nchunks);
+      f32x2 al2[E / 2], kk[E / 2];
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) {
+        kk[e] = *reinterpret_cast<const f32x2*>(k_s + t * K + col + 2 * e);
+        al2[e] = KDA ? *reinterpret_cast<const f32x2*>(g_s + t * K + col + 2 * e)
+                     : pack2(g_s[t], g_s[t]);
+      }
+#pragma unroll
+      for (int m = 0; m < G; ++m) {
+        if (FULL || cg + NT * m < nchunks) {
+          const float u = u_s[t * TILE_ROWS + (cg + NT * m) / CPR - row_base];
+          const f32x2 u2 = pack2(u, u);
+#pragma unroll
+          for (int e = 0; e < E / 2; ++e) x[m][e] = fold2(x[m][e], al2[e], u2, kk[e]);
+        }
+      }
       const long long pos = plan.p0 + t + 1;
       if (p.block_size > 0 && t + 1 < n && pos % p.block_size == 0) {
         const int bs = slot_after(trow, p.table_stride, p.block_size, pos);
-        store_chunks<ST, G, NT>(pool + ((size_t)bs * p.HV + h) * head, x, cg, nchunks);
+        ST* dst = pool + ((size_t)bs * p.HV + h) * head;
+#pragma unroll
+        for (int m = 0; m < G; ++m) {
+          const int c = cg + NT * m;
+          if (FULL || c < nchunks) C::store(dst + (size_t)c * E, x[m]);
+        }
       }
     }
-    store_chunks<ST, G, NT>(pool + ((size_t)plan.fin * p.HV + h) * head, x, cg, nchunks);
+#pragma unroll
+    for (int m = 0; m < G; ++m) {
+      const int c = cg + NT * m;
+      if (FULL || c < nchunks) C::store(pool + fin_off + (size_t)c * E, x[m]);
+    }
   }
 }
 
@@ -365,7 +394,8 @@ static int launch_commit_bf16_k(const CommitParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(float) * ((size_t)p.W * (TILE_ROWS + K) +
                                        (((size_t)p.W * (KDA ? K : 1) + 3) & ~(size_t)3)) +
                       (size_t)TILE_ROWS * K * sizeof(ST);
-  auto kern = gdn_commit_staged_kernel<K, ST, M, G, KDA>;
+  auto kern = p.V % TILE_ROWS == 0 ? gdn_commit_staged_kernel<K, ST, M, G, KDA, true>
+                                    : gdn_commit_staged_kernel<K, ST, M, G, KDA, false>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return GDN_ERR_CUDA;
