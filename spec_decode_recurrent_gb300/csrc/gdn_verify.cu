@@ -59,10 +59,12 @@ struct VerifyTile {
   // CTAs per SM the registers must allow, as measured: seven (72 registers)
   // for the native form and for the verify with a bf16 state; six (80
   // registers) for the verify with an fp32 state, which spills at 72.  The
-  // per-channel (KDA) gate holds eight more pairs per thread: five (96).
+  // per-channel (KDA) decay is applied before a token's keys and queries are
+  // loaded, so its gate registers are free again and it keeps the same
+  // budgets.
   template <bool NATIVE, typename ST, bool KDA>
   static constexpr int min_ctas() {
-    return KDA ? 5 : ((!NATIVE && sizeof(ST) == 4) ? 6 : 7);
+    return (!NATIVE && sizeof(ST) == 4) ? 6 : 7;
   }
 };
 
@@ -172,24 +174,35 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
     const f32x2 al2 = gq.x;  // (alpha, alpha)
     const float2 bk = unpack2(gq.y);
     const float be = bk.x, kq = bk.y;
-    f32x2 kk[8], qq[8], aa[KDA ? 8 : 1];
+    if constexpr (KDA) {
+      // H = S diag(alpha): each pair of this thread's columns by its own
+      // gates, applied before the keys and queries are loaded so that the
+      // gate registers are free again
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const ulonglong2 a4 = *reinterpret_cast<const ulonglong2*>(al_s + t * K + 4 * (l + LPR * m));
+#pragma unroll
+        for (int g = 0; g < RPT; ++g) {
+          s[g][2 * m] = mul2(s[g][2 * m], a4.x);
+          s[g][2 * m + 1] = mul2(s[g][2 * m + 1], a4.y);
+        }
+      }
+    }
+    f32x2 kk[8], qq[8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kh_s + t * K + 4 * (l + LPR * m));
       const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(qh_s + t * K + 4 * (l + LPR * m));
       kk[2 * m] = k4.x; kk[2 * m + 1] = k4.y;
       qq[2 * m] = q4.x; qq[2 * m + 1] = q4.y;
-      if constexpr (KDA) {
-        // the decay of this thread's own columns: S diag(alpha)
-        const ulonglong2 a4 = *reinterpret_cast<const ulonglong2*>(al_s + t * K + 4 * (l + LPR * m));
-        aa[2 * m] = a4.x; aa[2 * m + 1] = a4.y;
-      }
     }
 #pragma unroll
     for (int g = 0; g < RPT; ++g) {
-      // H = alpha * S
+      // H = alpha * S (the per-channel decay was applied above)
+      if constexpr (!KDA) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], KDA ? aa[KDA ? j : 0] : al2);
+        for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], al2);
+      }
       // d = H khat and H qhat in one pass: pair accumulators over pairs
       // 0-3 and 4-7, combined pairwise, lanes summed, then the LPR lanes
       f32x2 da = mul2(s[g][0], kk[0]), db = mul2(s[g][4], kk[4]);
