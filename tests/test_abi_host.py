@@ -130,3 +130,44 @@ def test_conv_commit_rejects_before_launch(lib):
     assert conv(bs=4) == -1                     # align mode needs seq_pos
     assert conv(ins=32) == -3                   # row stride shorter than C
     assert conv(L=0) == -3
+
+
+def test_kda_entry_points_reject_before_launch(lib):
+    # the per-channel (KDA) calls share the scalar-gate calls' checks and
+    # also want the [B][HV][W][K] gate record 16-byte aligned
+    def kda_verify(shape, **over):
+        args = dict(batch=2, T=8, slots=4, q=FAKE, qs=2048, k=FAKE, ks=2048, v=FAKE, vs=4096,
+                    a=FAKE, b=FAKE, A_log=FAKE, dt_bias=FAKE, ts=FAKE, wl=FAKE, pool=FAKE, st=FAKE,
+                    sts=1, sp=None, bs=0, out=FAKE, os=4096, ru=FAKE, rk=FAKE, rg=FAKE, err=None)
+        args.update(over)
+        sh = ctypes.byref(shape) if shape is not None else None
+        return lib.gdn_kda_spec_verify(sh, *[args[k] for k in (
+            "batch", "T", "slots", "q", "qs", "k", "ks", "v", "vs", "a", "b", "A_log", "dt_bias",
+            "ts", "wl", "pool", "st", "sts", "sp", "bs", "out", "os", "ru", "rk", "rg", "err")],
+            None)
+    assert kda_verify(None) == -1
+    assert kda_verify(_shape(), rg=None) == -1
+    assert kda_verify(_shape(head_k=96)) == -2
+    assert kda_verify(_shape(), qs=1024) == -3
+    assert kda_verify(_shape(), rg=ctypes.c_void_p((1 << 20) + 4)) == -3   # gate record 4-aligned only
+
+    sh = _shape()
+    args = [2, 8, 4, FAKE, 2048, FAKE, 2048, FAKE, 4096, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+            FAKE, 1, None, 0, FAKE, 4096]
+    assert lib.gdn_kda_native_spec_snapshot(ctypes.byref(sh), *args, None, None, None) == -1
+    assert lib.gdn_kda_native_spec_snapshot(ctypes.byref(sh), *args,
+                                            ctypes.c_void_p((1 << 20) + 4), None, None) == -3
+
+    def kda_commit(shape, **over):
+        a = dict(L=36, batch=4, slots=8, pools=FAKE, ru=FAKE, rk=FAKE, rg=FAKE, wl=FAKE,
+                 al=FAKE, st=FAKE, sts=1, sp=None, bs=0)
+        a.update(over)
+        sh_ = ctypes.byref(shape) if shape is not None else None
+        return lib.gdn_kda_replay_commit(sh_, *[a[k] for k in (
+            "L", "batch", "slots", "pools", "ru", "rk", "rg", "wl", "al", "st", "sts", "sp",
+            "bs")], None, None)
+    assert kda_commit(None) == -1
+    assert kda_commit(_shape(), rg=None) == -1
+    assert kda_commit(_shape(head_v=48)) == -2
+    assert kda_commit(_shape(), L=0) == -3
+    assert kda_commit(_shape(), bs=3) == -1
