@@ -32,6 +32,10 @@
 // Ordering: in both kernels every chunk of the tile is read before any of
 // it is written.
 //
+// Per-channel (KDA) records carry K gates per token; the fold then scales
+// each column by its own gate, S[i][j] = fma(u[i], khat[j], S[i][j] *
+// alpha[j]), in the same kernels (a compile-time flag).
+//
 // Rows the verify rejected (token rows out of range, or any other row
 // error) carry the reject marker in gate record position 0; both kernels
 // check it once the record is staged and store nothing for such a row, so

@@ -31,6 +31,9 @@
 // The two lane sums share their shuffles: one exchange leaves d on the lower
 // half of a row's lanes and o on the upper half, each half then sums its own
 // value, and d is broadcast back (4 shuffles per row and token, not 6).
+// With the per-channel (KDA) decay, H = S diag(alpha_t): the staging computes
+// one gate per (token, channel), and each thread scales its own columns by
+// their gates before the token's keys and queries are loaded.
 //
 // VERIFY mode writes o_t and the replay record (u_t, khat_t, alpha_t) and no
 // state (vLLM PR "[Spec Decode][Qwen4Exp] RecoverSSM for Qwen GDN and the
