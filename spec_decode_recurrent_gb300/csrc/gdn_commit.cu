@@ -27,7 +27,9 @@
 // ~128 KiB in flight.  bf16 states (gdn_commit_staged_kernel): one CTA per
 // whole head, the tile itself copied into shared memory with the record and
 // folded four chunks at a time, so four CTAs per SM again keep 128 KiB in
-// flight (a register-held bf16 tile would keep only half of that).
+// flight (a register-held bf16 tile would keep only half of that).  The
+// tile arrives in two commit groups, one per fold group, and the first is
+// folded while the second is still landing.
 //
 // Ordering: in both kernels every chunk of the tile is read before any of
 // it is written.
@@ -46,6 +48,13 @@
 #include "gdn_launch.h"
 
 namespace gdn {
+
+// Waits until at most N of this thread's most recent cp.async commit groups
+// are still in flight (a hardware wait, no polling).
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Slot-table row of request r for the group of `layer`, or NULL when the
 // layer's group id is outside [0, num_groups).
@@ -292,12 +301,24 @@ __global__ void __launch_bounds__(kCommitThreads, 4)
   const size_t head = (size_t)p.V * K;
   ST* pool = static_cast<ST*>(p.pools[layer]);
   const ST* S0 = pool + ((size_t)plan.src * p.HV + h) * head + (size_t)row_base * K;
-  for (int c = tid; c < rows * CPR; c += NT) cp_async16(tile_s + (size_t)c * E, S0 + (size_t)c * E);
-  cp_async_commit();
-  cp_async_wait_all();
+  // the tile in M / G commit groups, one per fold group: a thread copies
+  // exactly the chunks it later folds, so each group needs only the
+  // thread's own wait, and a group is folded while the later ones land
+  static_assert(M / G <= 2, "at most two fold groups per thread");
+#pragma unroll
+  for (int grp = 0; grp < M / G; ++grp) {
+#pragma unroll
+    for (int m = 0; m < G; ++m) {
+      const int c = tid + NT * (G * grp + m);  // chunk inside the tile
+      if (FULL || c < rows * CPR) cp_async16(tile_s + (size_t)c * E, S0 + (size_t)c * E);
+    }
+    cp_async_commit();
+  }
+  cp_async_wait_group<M / G - 1>();  // the record and the first fold group
   __syncthreads();
   if (g_s[0] < 0.f) {  // the verify rejected this row: nothing is stored
     if (p.err && tid == 0 && tile == 0 && h == 0) atomicOr(p.err, GDN_ROW_ERR_REJECTED);
+    cp_async_wait_all();
     return;
   }
 
@@ -308,6 +329,7 @@ __global__ void __launch_bounds__(kCommitThreads, 4)
   const size_t fin_off = ((size_t)plan.fin * p.HV + h) * head;
 #pragma unroll 1
   for (int grp = 0; grp < M / G; ++grp) {
+    if (grp > 0) cp_async_wait_all();  // the second fold group's own chunks
     const int cg = row_base * CPR + tid + NT * G * grp;  // first chunk of this group (head index)
     f32x2 x[G][E / 2];
 #pragma unroll
