@@ -48,11 +48,61 @@ def verify_all(sb: SpecBatch, bufs: StepBuffers, stream=None) -> None:
         verify_layer(sb, bufs, layer, stream)
 
 
-def commit(sb: SpecBatch, bufs: StepBuffers, stream=None) -> None:
+def commit(sb: SpecBatch, bufs: StepBuffers, stream=None, check_slots: bool = False) -> None:
+    """The all-layer commit.  check_slots (a debug aid: it copies the row
+    metadata to the host and synchronises) first verifies that no live row
+    writes a slot another live row reads or writes."""
+    if check_slots:
+        check_slot_exclusivity(sb.window_len, sb.accepted_len, sb.slot_table, sb.seq_pos,
+                               sb.block_size)
     api.gdn_replay_commit(table=bufs.table, num_k_heads=sb.HK, window_len=sb.window_len,
                           accepted_len=sb.accepted_len, slot_table=sb.slot_table,
                           seq_pos=sb.seq_pos, block_size=sb.block_size, err=bufs.err,
                           stream=stream)
+
+
+def check_slot_exclusivity(window_len, accepted_len, slot_table, seq_pos=None,
+                           block_size: int = 0) -> None:
+    """Raise ValueError if a slot one live row of a commit writes (its final
+    or a boundary slot) is read or written by another live row: the rows of
+    one launch run concurrently with no ordering between them, so such a
+    call has no defined result.  A row may write its own checkpoint slot.
+    Rows the commit would skip or flag (null slot, nothing accepted, a
+    malformed row) are left out.  Host-side, for debugging."""
+    win = [int(x) for x in window_len.tolist()]
+    acc = [int(x) for x in accepted_len.tolist()]
+    table = slot_table.view(len(win), -1).tolist()
+    pos = [int(x) for x in seq_pos.tolist()] if (block_size and seq_pos is not None) else None
+
+    def slot_after(row, x):
+        if block_size == 0:
+            return row[0]
+        col = (x - 1) // block_size
+        return row[col] if 1 <= x and col < len(row) else None
+
+    reads, writes = {}, {}
+    for r, (w, n) in enumerate(zip(win, acc)):
+        if w <= 0 or n <= 0 or n > w:
+            continue
+        p0 = pos[r] if pos is not None else 0
+        src = slot_after(table[r], p0)
+        if src is None or src < 0:
+            continue
+        mine = set()
+        for j in range(1, n + 1):           # the block of every accepted token
+            if block_size == 0 and j < n:
+                continue
+            s_ = slot_after(table[r], p0 + j)
+            if s_ is not None and s_ >= 0:
+                mine.add(s_)
+        reads.setdefault(src, set()).add(r)
+        for s_ in mine:
+            writes.setdefault(s_, set()).add(r)
+    for s_, rows in writes.items():
+        others = (rows | reads.get(s_, set()))
+        if len(others) > 1:
+            raise ValueError(f"slot {s_} is written by row(s) {sorted(rows)} and used by rows "
+                             f"{sorted(others)} in the same commit")
 
 
 def native_layer(sb: SpecBatch, layer: int, out: torch.Tensor, snapshots: torch.Tensor,

@@ -131,3 +131,26 @@ def test_mtp5_acceptance_profile_matches_the_measured_rates():
     assert bool((acc >= 1).all() and (acc <= 6).all())
     assert bool((sb.accepted_len[~live] == 0).all())
 
+
+
+def test_slot_exclusivity_check():
+    from spec_decode_recurrent_gb300 import step
+    # every benchmark workload commits to disjoint slots
+    for sb in (wl.all_layer(L=1, batch=10, pad_rows=2, HK=2, HV=4, KV=16, num_slots=16),
+               wl.align(L=1, batch=32, HK=1, HV=2, KV=16, num_slots=80),
+               wl.long_ragged(L=1, batch=12, HK=2, HV=4, KV=16, num_slots=24)):
+        step.check_slot_exclusivity(sb.window_len, sb.accepted_len, sb.slot_table, sb.seq_pos,
+                                    sb.block_size)
+    i32 = lambda x: torch.tensor(x, dtype=torch.int32)
+    # two rows writing the same slot in place
+    with pytest.raises(ValueError, match="slot 3"):
+        step.check_slot_exclusivity(i32([4, 4]), i32([2, 1]), i32([[3], [3]]))
+    # a null row, or a row with nothing accepted, may share (it writes nothing)
+    step.check_slot_exclusivity(i32([4, 4]), i32([2, 0]), i32([[3], [3]]))
+    step.check_slot_exclusivity(i32([4, 4]), i32([2, 1]), i32([[3], [-1]]))
+    # align mode: row 0's boundary slot is row 1's checkpoint slot
+    with pytest.raises(ValueError, match="slot 7"):
+        step.check_slot_exclusivity(i32([4, 4]), i32([4, 1]), i32([[5, 7, 8], [7, 9, -1]]),
+                                    i32([4, 4]), 4)
+    # a row may write its own checkpoint slot (boundary = source)
+    step.check_slot_exclusivity(i32([4]), i32([3]), i32([[5, 6, 7]]), i32([6]), 4)
