@@ -301,3 +301,27 @@ def test_graph_captured_step_matches_eager_bitwise():
         assert torch.equal(bufs.out[l].view(torch.int32), eager.out[l].view(torch.int32))
         assert torch.equal(bufs.rec_u[l].view(torch.int32), eager.rec_u[l].view(torch.int32))
         assert torch.equal(sb.pools[l].view(torch.int32), eager_pools[l].view(torch.int32))
+
+
+@pytest.mark.parametrize("kda", [False, True])
+def test_verify_writes_into_a_strided_output_view(kda):
+    # The verify writes o_t straight into the layer's output, which may be a
+    # slice of a wider buffer (vLLM PR, Commits item 2: out=): the strided
+    # result equals the contiguous one bit for bit, and the columns between
+    # rows stay untouched.
+    sb = wl.custom(device="cuda", kda=kda, HK=2, HV=4, K=128, V=128, W=4, L=1,
+                   windows=[4, 2, 3], accepted=[2, 2, 3], qkv_dtype=wl.BF16)
+    ref = step.StepBuffers(sb, fill=float("nan"))
+    step.verify_all(sb, ref)
+    pad = 96
+    wide = torch.full((sb.T, sb.HV * sb.V + pad), float("nan"), device="cuda")
+    view = wide[:, :sb.HV * sb.V].view(sb.T, sb.HV, sb.V)
+    assert view.stride(0) == sb.HV * sb.V + pad
+    bufs = step.StepBuffers(sb, fill=float("nan"))
+    bufs.out[0] = view
+    step.verify_all(sb, bufs)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(view.contiguous()), bits(ref.out[0]))
+    assert torch.isnan(wide[:, sb.HV * sb.V:]).all()
+    for name in ("rec_u", "rec_k", "rec_g"):
+        assert torch.equal(bits(getattr(bufs, name)[0]), bits(getattr(ref, name)[0]))
