@@ -335,6 +335,22 @@ int gdn_kda_replay_commit(const gdn_shape* shape, int32_t num_layers,
                           const int32_t* seq_pos, int32_t block_size,
                           int32_t* err, void* stream);
 
+/* The grouped all-layer commit (arguments as gdn_replay_commit_grouped) with
+ * per-channel gate records [batch][HV][W][K]. */
+int gdn_kda_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers,
+                                  int32_t num_groups, const int32_t* layer_group,
+                                  int32_t batch, int32_t num_slots,
+                                  void* const* state_pools,
+                                  const float* const* rec_u,
+                                  const float* const* rec_k,
+                                  const float* const* rec_g,
+                                  const int32_t* window_len,
+                                  const int32_t* accepted_len,
+                                  const int32_t* slot_tables,
+                                  int32_t slot_table_stride, int64_t group_stride,
+                                  const int32_t* seq_pos, int32_t block_size,
+                                  int32_t* err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,8 @@ ROW_ERR_BLOCK, ROW_ERR_SEQPOS, ROW_ERR_TOKENS = 8, 16, 32
 ROW_ERR_GROUP, ROW_ERR_REJECTED = 64, 128
 ENTRY_POINTS = ("gdn_spec_verify", "gdn_replay_commit", "gdn_replay_commit_grouped",
                 "gdn_conv_state_commit", "gdn_native_spec_snapshot", "gdn_kda_spec_verify",
-                "gdn_kda_native_spec_snapshot", "gdn_kda_replay_commit")
+                "gdn_kda_native_spec_snapshot", "gdn_kda_replay_commit",
+                "gdn_kda_replay_commit_grouped")
 
 _ERRORS = {-1: "null pointer", -2: "unsupported shape or dtype",
            -3: "invalid count, stride, alignment or block size", -4: "CUDA launch failed"}
@@ -85,6 +86,8 @@ def load() -> ctypes.CDLL:
             lib.gdn_replay_commit_grouped.argtypes = [
                 ctypes.POINTER(gdn_shape), _I32, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
                 _P, _I32, _I64, _P, _I32, _P, _P]
+            lib.gdn_kda_replay_commit_grouped.restype = ctypes.c_int
+            lib.gdn_kda_replay_commit_grouped.argtypes = lib.gdn_replay_commit_grouped.argtypes
             _lib = lib
     return _lib
 
@@ -295,8 +298,8 @@ def gdn_replay_commit_grouped(*, table: LayerTable, num_k_heads: int, layer_grou
                               accepted_len, slot_tables, seq_pos=None, block_size=0, err=None,
                               stream=None) -> None:
     """All-layer commit in one launch for layers split into KV-cache groups:
-    layer l uses slot_tables[layer_group[l]] ([groups, batch, stride])."""
-    _need(not table.kda, "the grouped commit takes scalar-gate records")
+    layer l uses slot_tables[layer_group[l]] ([groups, batch, stride]).  A
+    table of per-channel gate records (KDA) calls gdn_kda_replay_commit_grouped."""
     B = window_len.shape[0]
     _need(B == table.B, "batch must match the record buffers")
     for name, t in (("window_len", window_len), ("accepted_len", accepted_len)):
@@ -313,13 +316,14 @@ def gdn_replay_commit_grouped(*, table: LayerTable, num_k_heads: int, layer_grou
     G, _, stride = slot_tables.shape
     shape = gdn_shape(int(num_k_heads), table.HV, table.K, table.V, table.W, GDN_DTYPE_F32,
                       _dtype_code(table.state_dtype))
-    rc = load().gdn_replay_commit_grouped(
+    fn = "gdn_kda_replay_commit_grouped" if table.kda else "gdn_replay_commit_grouped"
+    rc = getattr(load(), fn)(
         ctypes.byref(shape), table.num_layers, G, _ptr(layer_group), B, table.num_slots,
         _ptr(table.d_pools), _ptr(table.d_rec_u), _ptr(table.d_rec_k), _ptr(table.d_rec_g),
         _ptr(window_len), _ptr(accepted_len), _ptr(slot_tables), stride, B * stride,
         _ptr(seq_pos if block_size else None), int(block_size), _ptr(err), _stream(stream))
     if rc != 0:
-        raise GDNError("gdn_replay_commit_grouped", rc)
+        raise GDNError(fn, rc)
 
 
 class ConvTable:

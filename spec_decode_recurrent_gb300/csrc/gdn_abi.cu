@@ -258,6 +258,20 @@ int gdn_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
                        seq_pos, block_size, err, stream, false);
 }
 
+int gdn_kda_replay_commit_grouped(const gdn_shape* shape, int32_t num_layers,
+                                  int32_t num_groups, const int32_t* layer_group, int32_t batch,
+                                  int32_t num_slots, void* const* state_pools,
+                                  const float* const* rec_u, const float* const* rec_k,
+                                  const float* const* rec_g, const int32_t* window_len,
+                                  const int32_t* accepted_len, const int32_t* slot_tables,
+                                  int32_t slot_table_stride, int64_t group_stride,
+                                  const int32_t* seq_pos, int32_t block_size, int32_t* err,
+                                  void* stream) {
+  return commit_common(shape, num_layers, num_groups, layer_group, batch, num_slots, state_pools,
+                       rec_u, rec_k, rec_g, window_len, accepted_len, slot_tables,
+                       slot_table_stride, group_stride, seq_pos, block_size, err, stream, true);
+}
+
 int gdn_kda_replay_commit(const gdn_shape* shape, int32_t num_layers, int32_t batch,
                           int32_t num_slots, void* const* state_pools,
                           const float* const* rec_u, const float* const* rec_k,

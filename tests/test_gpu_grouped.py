@@ -134,3 +134,60 @@ def test_bad_group_id_is_flagged_and_writes_nothing():
     torch.cuda.synchronize()
     assert int(bufs.err.item()) == api.ROW_ERR_GROUP
     assert torch.equal(bits(sb.pools[2]), bits(before))
+
+
+def test_kda_grouped_commit_matches_native_and_oracle():
+    # The per-channel-decay (KDA) records through the grouped commit: bit
+    # for bit the native KDA snapshots of every layer under its group's
+    # table, and within tolerance of the oracle's KDA commit of that layer.
+    G, L, seed = 3, 6, 8
+    sb = wl.custom(device="cuda", sentinel=False, seed=seed, kda=True, HK=2, HV=4, K=128, V=128,
+                   W=4, L=L, windows=[4, 3, 4, 1, 0, 4], accepted=[2, 3, 4, 1, 0, 1], num_slots=24)
+    gen = torch.Generator().manual_seed(seed)
+    tables = [sb.slot_table.cpu()] + [
+        torch.randperm(sb.num_slots, generator=gen)[:sb.B].view(-1, 1).to(torch.int32)
+        for _ in range(1, G)]
+    slot_tables = torch.stack(tables).to("cuda").contiguous()
+    layer_group = torch.tensor([l % G for l in range(L)], dtype=torch.int32, device="cuda")
+    before = [p.clone() for p in sb.pools]
+    bufs = step.StepBuffers(sb, fill=NAN)
+    expected = []
+    for l in range(L):
+        g = int(layer_group[l])
+        kw = dict(q=sb.q[l], k=sb.k[l], v=sb.v[l], a=sb.a[l], b=sb.b[l], A_log=sb.A_log[l],
+                  dt_bias=sb.dt_bias[l], token_start=sb.token_start, window_len=sb.window_len,
+                  state_pool=sb.pools[l], slot_table=slot_tables[g], max_window=sb.W)
+        api.gdn_kda_spec_verify(out=bufs.out[l], rec_u=bufs.rec_u[l], rec_k=bufs.rec_k[l],
+                                rec_g=bufs.rec_g[l], err=bufs.err, **kw)
+        out, snaps = step.native_buffers(sb, fill=NAN)
+        api.gdn_kda_native_spec_snapshot(out=out, snapshots=snaps, **kw)
+        exp = sb.pools[l].clone()
+        for r in range(sb.B):
+            src, writes = oracle.commit_plan(int(sb.window_len[r]), int(sb.accepted_len[r]),
+                                             slot_tables[g, r].cpu(), 0, 0, sb.num_slots, sb.W)
+            for slot, ntok in writes:
+                exp[slot] = snaps[r, ntok - 1]
+        expected.append(exp)
+    api.gdn_replay_commit_grouped(table=bufs.table, num_k_heads=sb.HK, layer_group=layer_group,
+                                  window_len=sb.window_len, accepted_len=sb.accepted_len,
+                                  slot_tables=slot_tables, err=bufs.err)
+    torch.cuda.synchronize()
+    assert int(bufs.err.item()) == 0
+    for l in range(L):
+        assert torch.equal(bits(sb.pools[l]), bits(expected[l])), f"layer {l}"
+        g = int(layer_group[l])
+        rec = oracle.kda_spec_verify(
+            q=sb.q[l].cpu(), k=sb.k[l].cpu(), v=sb.v[l].cpu(), a=sb.a[l].cpu(), b=sb.b[l].cpu(),
+            A_log=sb.A_log[l].cpu(), dt_bias=sb.dt_bias[l].cpu(), token_start=sb.token_start.cpu(),
+            window_len=sb.window_len.cpu(), pool=before[l].cpu(), slot_table=slot_tables[g].cpu(),
+            max_window=sb.W)
+        pools, err = oracle.kda_replay_commit(
+            pools=cpu64(before[l])[None], rec_u=rec["rec_u"][None], rec_k=rec["rec_k"][None],
+            rec_g=rec["rec_g"][None], window_len=sb.window_len.cpu(),
+            accepted_len=sb.accepted_len.cpu(), slot_table=slot_tables[g].cpu(), max_window=sb.W)
+        assert np.all(err == 0)
+        got, ref, was = cpu64(sb.pools[l]), pools[0], cpu64(before[l])
+        changed = ref != was
+        assert changed.any()
+        assert np.array_equal(got[~changed], was[~changed])
+        check_close(got[changed], ref[changed], f"layer {l} KDA grouped commit")
