@@ -133,6 +133,20 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
   x[2] = bf16_bits_to_float(t.y & 0xffffu);
   x[3] = bf16_bits_to_float(t.y >> 16);
 }
+// A 16-byte piece of elements widened exactly to fp32: four fp32 values, or
+// eight bf16 values (lower half-word first).
+__device__ __forceinline__ void widen16(const uint4& t, float (&x)[4]) {
+  x[0] = __uint_as_float(t.x); x[1] = __uint_as_float(t.y);
+  x[2] = __uint_as_float(t.z); x[3] = __uint_as_float(t.w);
+}
+__device__ __forceinline__ void widen16(const uint4& t, float (&x)[8]) {
+  const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16_bits_to_float(w[i] & 0xffffu);
+    x[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+  }
+}
 __device__ __forceinline__ float load1(const float* p) { return *p; }
 __device__ __forceinline__ float load1(const __nv_bfloat16* p) {
   return bf16_bits_to_float(*reinterpret_cast<const unsigned short*>(p));

@@ -174,7 +174,7 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
   auto token = [&](int t, auto update_tag) {
     constexpr bool UPDATE = decltype(update_tag)::value;
     const ulonglong2 gq = *reinterpret_cast<const ulonglong2*>(gs_s + 4 * t);
-    const f32x2 al2 = gq.x;  // (alpha, alpha)
+    [[maybe_unused]] const f32x2 al2 = gq.x;  // (alpha, alpha); unused with the KDA decay
     const float2 bk = unpack2(gq.y);
     const float be = bk.x, kq = bk.y;
     if constexpr (KDA) {
@@ -324,7 +324,11 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   }
 
   // ---- stage normalised keys / queries, their dot product, the gates and
-  // ---- the value rows of all NS tiles for the whole window in shared memory
+  // ---- the value rows of all NS tiles for the whole window in shared
+  // ---- memory.  Every global load of the stage is issued before any of its
+  // ---- arithmetic or shared-memory stores, so the stage costs one memory
+  // ---- round trip after the row plan's instead of one per loop pass (a
+  // ---- load is not moved above an earlier pass's stores by the compiler).
   constexpr int SV = NS * VT;           // staged value rows
   float* kh_s = reinterpret_cast<float*>(smem_raw + 16 + kTileBytes);  // [W][K]
   float* qh_s = kh_s + p.W * K;         // [W][K]
@@ -334,76 +338,161 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   const QKV* qb = static_cast<const QKV*>(p.q);
   const QKV* kb = static_cast<const QKV*>(p.k);
   const QKV* vb = static_cast<const QKV*>(p.v);
-  for (int t = warp; t < w; t += Tile::WARPS) {
-    const long long row_t = t0 + t;
-    float kx[4] = {0.f, 0.f, 0.f, 0.f}, qx[4] = {0.f, 0.f, 0.f, 0.f};
-    if (lane < K / 4) {
-      load4(kb + row_t * p.k_stride + (size_t)hk * K + 4 * lane, kx);
-      load4(qb + row_t * p.q_stride + (size_t)hk * K + 4 * lane, qx);
-    }
-    float ks = __fmul_rn(kx[0], kx[0]), qs = __fmul_rn(qx[0], qx[0]);
+
+  // value rows as 16-byte pieces when whole tiles and 16-byte aligned rows
+  // allow it: piece c covers values [VE c, VE c + VE) of v_s ([W][SV])
+  constexpr int VE = 16 / sizeof(QKV);  // values per piece
+  constexpr int VPT = SV / VE;          // pieces per token
+  const int vpieces = w * VPT;
+  const bool vvec = FULL && (reinterpret_cast<uintptr_t>(vb) & 15) == 0 &&
+                    ((size_t)p.v_stride * sizeof(QKV)) % 16 == 0;
+  const QKV* vrow0 = vb + t0 * p.v_stride + (size_t)h * p.V + (size_t)tile0 * VT;
+  auto v_piece = [&](int c) {
+    return *reinterpret_cast<const uint4*>(vrow0 + (long long)(c / VPT) * p.v_stride + (c % VPT) * VE);
+  };
+  uint4 vr[2] = {};
+  if (vvec) {
 #pragma unroll
-    for (int e = 1; e < 4; ++e) {
-      ks = __fmaf_rn(kx[e], kx[e], ks);
-      qs = __fmaf_rn(qx[e], qx[e], qs);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      ks = __fadd_rn(ks, __shfl_xor_sync(0xffffffffu, ks, off));
-      qs = __fadd_rn(qs, __shfl_xor_sync(0xffffffffu, qs, off));
-    }
-    // x / sqrt(|x|^2 + eps) as x * rsqrt(|x|^2 + eps), rsqrt correctly rounded
-    const float kr = __frsqrt_rn(__fadd_rn(ks, kL2NormEps));
-    const float qr = __frsqrt_rn(__fadd_rn(qs, kL2NormEps));
-    float kn[4], qn[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      kn[e] = __fmul_rn(kx[e], kr);
-      qn[e] = __fmul_rn(qx[e], qr);
-    }
-    float kq = __fmul_rn(kn[0], qn[0]);
-#pragma unroll
-    for (int e = 1; e < 4; ++e) kq = __fmaf_rn(kn[e], qn[e], kq);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) kq = __fadd_rn(kq, __shfl_xor_sync(0xffffffffu, kq, off));
-    if (lane < K / 4) {
-      *reinterpret_cast<float4*>(kh_s + t * K + 4 * lane) = make_float4(kn[0], kn[1], kn[2], kn[3]);
-      *reinterpret_cast<float4*>(qh_s + t * K + 4 * lane) = make_float4(qn[0], qn[1], qn[2], qn[3]);
-    }
-    if (lane == 0) gs_s[4 * t + 3] = kq;
+    for (int j = 0; j < 2; ++j)
+      if (tid + j * Tile::THREADS < vpieces) vr[j] = v_piece(tid + j * Tile::THREADS);
   }
-  // gates of the whole window: one lane per token in the last warp; the
-  // per-channel decay (KDA) one element per thread: a [T][HV][K],
-  // dt_bias [HV][K]
-  if (warp == Tile::WARPS - 1 && lane < w) {
+  // gate inputs of the whole window: one lane per token in the last warp
+  const bool glane = warp == Tile::WARPS - 1 && lane < w;
+  float g_a = 0.f, g_b = 0.f, g_Alog = 0.f, g_dt = 0.f;
+  if (glane) {
     const size_t gi = (size_t)(t0 + lane) * p.HV + h;
     if constexpr (!KDA) {
-      const float al = gate_decay(p.a[gi], p.A_log[h], p.dt_bias[h]);
+      g_a = p.a[gi];
+      g_Alog = p.A_log[h];
+      g_dt = p.dt_bias[h];
+    }
+    g_b = p.b[gi];
+  }
+  // per-channel decay inputs (KDA): a [T][HV][K], dt_bias [HV][K], four
+  // channels per thread and pass when both are 16-byte aligned
+  const int kpieces = w * (K / 4);
+  const bool kvec = KDA && ((reinterpret_cast<uintptr_t>(p.a) | reinterpret_cast<uintptr_t>(p.dt_bias)) & 15) == 0;
+  auto decay_in = [&](int c, float4& av, float4& dv) {
+    const int t = c / (K / 4), j = 4 * (c % (K / 4));
+    av = *reinterpret_cast<const float4*>(p.a + ((size_t)(t0 + t) * p.HV + h) * K + j);
+    dv = *reinterpret_cast<const float4*>(p.dt_bias + (size_t)h * K + j);
+  };
+  float4 ka = {}, kd = {};
+  float kAlog = 0.f;
+  if constexpr (KDA) {
+    kAlog = p.A_log[h];
+    if (kvec && tid < kpieces) decay_in(tid, ka, kd);
+  }
+
+  // keys and queries: two tokens per warp and pass (eight per CTA)
+  for (int tb = 0; tb < w; tb += 2 * Tile::WARPS) {
+    float kx[2][4], qx[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int t = tb + warp + j * Tile::WARPS;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) kx[j][e] = qx[j][e] = 0.f;
+      if (t < w && lane < K / 4) {
+        load4(kb + (t0 + t) * p.k_stride + (size_t)hk * K + 4 * lane, kx[j]);
+        load4(qb + (t0 + t) * p.q_stride + (size_t)hk * K + 4 * lane, qx[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int t = tb + warp + j * Tile::WARPS;
+      if (t >= w) break;  // warp-uniform
+      float ks = __fmul_rn(kx[j][0], kx[j][0]), qs = __fmul_rn(qx[j][0], qx[j][0]);
+#pragma unroll
+      for (int e = 1; e < 4; ++e) {
+        ks = __fmaf_rn(kx[j][e], kx[j][e], ks);
+        qs = __fmaf_rn(qx[j][e], qx[j][e], qs);
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        ks = __fadd_rn(ks, __shfl_xor_sync(0xffffffffu, ks, off));
+        qs = __fadd_rn(qs, __shfl_xor_sync(0xffffffffu, qs, off));
+      }
+      // x / sqrt(|x|^2 + eps) as x * rsqrt(|x|^2 + eps), rsqrt correctly rounded
+      const float kr = __frsqrt_rn(__fadd_rn(ks, kL2NormEps));
+      const float qr = __frsqrt_rn(__fadd_rn(qs, kL2NormEps));
+      float kn[4], qn[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kn[e] = __fmul_rn(kx[j][e], kr);
+        qn[e] = __fmul_rn(qx[j][e], qr);
+      }
+      float kq = __fmul_rn(kn[0], qn[0]);
+#pragma unroll
+      for (int e = 1; e < 4; ++e) kq = __fmaf_rn(kn[e], qn[e], kq);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) kq = __fadd_rn(kq, __shfl_xor_sync(0xffffffffu, kq, off));
+      if (lane < K / 4) {
+        *reinterpret_cast<float4*>(kh_s + t * K + 4 * lane) = make_float4(kn[0], kn[1], kn[2], kn[3]);
+        *reinterpret_cast<float4*>(qh_s + t * K + 4 * lane) = make_float4(qn[0], qn[1], qn[2], qn[3]);
+      }
+      if (lane == 0) gs_s[4 * t + 3] = kq;
+    }
+  }
+  // gates
+  if (glane) {
+    if constexpr (!KDA) {
+      const float al = gate_decay(g_a, g_Alog, g_dt);
       gs_s[4 * lane] = al;
       gs_s[4 * lane + 1] = al;
     }
-    gs_s[4 * lane + 2] = gate_beta(p.b[gi]);
+    gs_s[4 * lane + 2] = gate_beta(g_b);
   }
   if constexpr (KDA) {
-    const float A = expf(p.A_log[h]);  // once per head, not per channel
-    for (int i = tid; i < w * K; i += Tile::THREADS) {
-      const int t = i / K, j = i % K;
-      al_s[i] = gate_decay_scaled(p.a[((size_t)(t0 + t) * p.HV + h) * K + j], A,
-                                  p.dt_bias[(size_t)h * K + j]);
+    const float A = expf(kAlog);  // once per head, not per channel
+    if (kvec) {
+      auto put = [&](int c, const float4& av, const float4& dv) {
+        *reinterpret_cast<float4*>(al_s + 4 * c) =
+            make_float4(gate_decay_scaled(av.x, A, dv.x), gate_decay_scaled(av.y, A, dv.y),
+                        gate_decay_scaled(av.z, A, dv.z), gate_decay_scaled(av.w, A, dv.w));
+      };
+      if (tid < kpieces) put(tid, ka, kd);
+      for (int c = tid + Tile::THREADS; c < kpieces; c += Tile::THREADS) {
+        float4 av, dv;
+        decay_in(c, av, dv);
+        put(c, av, dv);
+      }
+    } else {
+      for (int i = tid; i < w * K; i += Tile::THREADS) {
+        const int t = i / K, j = i % K;
+        al_s[i] = gate_decay_scaled(p.a[((size_t)(t0 + t) * p.HV + h) * K + j], A,
+                                    p.dt_bias[(size_t)h * K + j]);
+      }
     }
   }
-  // the value rows of this CTA's tiles, every token, all threads
-  for (int i = tid; i < w * SV; i += Tile::THREADS) {
-    const int t = i / SV, row = tile0 * VT + i % SV;
-    v_s[i] = (FULL || row < p.V) ? load1(vb + (t0 + t) * p.v_stride + (size_t)h * p.V + row) : 0.f;
+  // the value rows of this CTA's tiles, every token
+  if (vvec) {
+    auto put = [&](int c, const uint4& x) {
+      float f[VE];
+      widen16(x, f);
+#pragma unroll
+      for (int e = 0; e < VE; e += 4)
+        *reinterpret_cast<float4*>(v_s + VE * c + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+    };
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (tid + j * Tile::THREADS < vpieces) put(tid + j * Tile::THREADS, vr[j]);
+    for (int c = tid + 2 * Tile::THREADS; c < vpieces; c += Tile::THREADS) put(c, v_piece(c));
+  } else {
+    for (int i = tid; i < w * SV; i += Tile::THREADS) {
+      const int t = i / SV, row = tile0 * VT + i % SV;
+      v_s[i] = (FULL || row < p.V) ? load1(vb + (t0 + t) * p.v_stride + (size_t)h * p.V + row) : 0.f;
+    }
   }
   __syncthreads();
 
   const size_t rec_base = ((size_t)r * p.HV + h) * p.W;  // record position 0
   if (!NATIVE && span == 0) {
-    for (int i = tid; i < w * K; i += Tile::THREADS) p.rec_k[rec_base * K + i] = kh_s[i];
+    // records are 16-byte aligned and K is a multiple of 4
+    for (int i = tid; i < w * K / 4; i += Tile::THREADS)
+      reinterpret_cast<float4*>(p.rec_k + rec_base * K)[i] = reinterpret_cast<const float4*>(kh_s)[i];
     if constexpr (KDA) {
-      for (int i = tid; i < w * K; i += Tile::THREADS) p.rec_g[rec_base * K + i] = al_s[i];
+      for (int i = tid; i < w * K / 4; i += Tile::THREADS)
+        reinterpret_cast<float4*>(p.rec_g + rec_base * K)[i] = reinterpret_cast<const float4*>(al_s)[i];
     } else {
       if (tid < w) p.rec_g[rec_base + tid] = gs_s[4 * tid];
     }
