@@ -1,48 +1,42 @@
 // gdn_verify.cu -- speculative verify and native per-draft snapshot kernels.
 //
-// One CTA of 4 warps runs the whole draft window over up to four tiles of VT
-// state rows (32 for K = 128) of one (request row, value head), one tile
-// after another, with the tile held in registers (tokenspeed PR "feat: add
-// Qwen3.5 GDN ReplaySSM", Summary and Implementation: a cooperative 4-warp
-// CTA per 128x128 state head).  The window's normalised keys and queries,
-// gates and values are staged once per CTA for all of its tiles: that
-// staging and the row plan cost as many instructions as the recurrence of
-// one tile, so a head run as four separate tile CTAs paid them four times.
-// Tiles reach the CTA as single bulk copies (cp.async.bulk, one thread, one
-// instruction per 16 KiB tile) into one shared-memory buffer, completed
-// through an mbarrier: tile i + 1 is requested as soon as every warp has
-// moved tile i into registers, so it streams in while tile i runs (80
-// registers and six CTAs per SM for an fp32 state, 72 and seven for bf16).
-// A CTA with a single tile (the native form) loads it straight into
-// registers.  Rows of S are independent given (khat, qhat, alpha, beta,
-// v_i), so tiles never communicate; the only reductions are over K, inside
-// a group of K/16 lanes, by warp shuffles.
+// The window in matrix form.  With the checkpoint C and the gate products
+// gamma_t = alpha_0 ... alpha_t and rho_{t,j} = alpha_{j+1} ... alpha_t
+// (per channel for the KDA decay), the state after token t is
+//   S_t = C diag(gamma_t) + sum_{j<=t} u_j (rho_{t,j} khat_j)^T,
+// so the two products the recurrence needs from H_t = alpha_t S_{t-1} are
+//   d_t = H_t khat_t = C kt_t + sum_{j<t}  A_{t,j} u_j,   kt_t = gamma_t khat_t,
+//   o_t = S_t qhat_t = C qt_t + sum_{j<=t} B_{t,j} u_j,   qt_t = gamma_t qhat_t,
+// with A_{t,j} = <rho_{t,j} khat_j, khat_t> and B_{t,j} = <rho_{t,j} khat_j,
+// qhat_t>, and u_t = beta_t (v_t - d_t) (tokenspeed PR "feat: add Qwen3.5 GDN
+// ReplaySSM", Summary; vLLM PR "[Spec Decode][Qwen4Exp] RecoverSSM for Qwen
+// GDN and the PLE short conv", Purpose).  The same d_t, u_t and o_t as the
+// token-by-token recurrence in exact arithmetic; what it changes is the
+// work per state element: 2w products against the checkpoint, all
+// independent, instead of a decay, two dot products and a rank-1 update per
+// token in a serial chain.  The window's side (kt, qt, A, B: O(w^2 K)) is
+// computed once per CTA.
 //
-// Register layout of a tile, for K = 128: LPR = 8 lanes share one state row
-// and each lane holds 16 of its columns, as four 4-column chunks at columns
-// 4 * (l + LPR * m), m = 0..3, kept as eight packed fp32 pairs; a warp's
-// load of chunk m reads whole 128-byte lines.  A warp covers RPW = 32 / LPR
-// rows per row group and each thread keeps RPT row groups.
-//
-// Per token: H = alpha * S; both dot products are taken in one pass over H,
-// d = H khat and H qhat; then u = beta * (v - d), S = H + u khat^T and
-// o = S qhat evaluated as H qhat + u * (khat . qhat), the same value in
-// exact arithmetic with the output off the state update's critical path.
-// The two lane sums share their shuffles: one exchange leaves d on the lower
-// half of a row's lanes and o on the upper half, each half then sums its own
-// value, and d is broadcast back (4 shuffles per row and token, not 6).
-// With the per-channel (KDA) decay, H = S diag(alpha_t): the staging computes
-// one gate per (token, channel), and each thread scales its own columns by
-// their gates before the token's keys and queries are loaded.
+// One CTA of 4 warps covers up to four tiles of VT state rows (32 for
+// K = 128) of one (request row, value head), the tile held in registers, a
+// cooperative 4-warp CTA per 128x128 state head (tokenspeed PR,
+// Implementation).  Per tile and token each lane forms its partial products
+// with kt_t and qt_t; the LPR lanes of a row combine them by recursive
+// halving (each exchange sends half of the remaining values and keeps the
+// other half), and the row sums land in shared memory.  After the last tile
+// one thread per row runs the short scalar recurrence for u_t and o_t and
+// writes both, coalesced.  Tiles reach the CTA as single bulk copies
+// (cp.async.bulk, one thread per 16 KiB tile) into a shared buffer, completed
+// through an mbarrier; tile i + 1 is requested as soon as every warp has
+// moved tile i into registers.
 //
 // VERIFY mode writes o_t and the replay record (u_t, khat_t, alpha_t) and no
-// state (vLLM PR "[Spec Decode][Qwen4Exp] RecoverSSM for Qwen GDN and the
-// PLE short conv", Purpose).  NATIVE mode writes o_t and the full state after
-// every token instead, one tile per CTA.  Both run the identical per-token
-// arithmetic on every row, so their outputs agree bit for bit however the
-// tiles are grouped into CTAs, and the state update is the commit's fold
-// (which VERIFY mode skips after the window's last token: that state is
-// never read).
+// state.  NATIVE mode (one tile per CTA) computes the same u_t and o_t the
+// same way, then folds the tile token by token with the commit's update,
+// S_t = fma(u_t, khat_t, S_{t-1} * alpha_t), and writes every S_t.  So the
+// verify's outputs equal the native ones bit for bit, and a commit of n
+// accepted tokens (the same fold over the verify's records) equals the
+// native state after token n.
 #include <type_traits>
 
 #include "gdn_async.cuh"
@@ -59,31 +53,48 @@ struct VerifyTile {
   static constexpr int WARPS = 4;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int VT = WARPS * RPW * RPT;    // state rows per tile
-  // CTAs per SM the registers must allow, as measured: seven (72 registers)
-  // for the native form and for the verify with a bf16 state; six (80
-  // registers) for the verify with an fp32 state, which spills at 72.  The
-  // per-channel (KDA) decay is applied before a token's keys and queries are
-  // loaded, so its gate registers are free again and it keeps the same
-  // budgets.
   template <bool NATIVE, typename ST, bool KDA>
   static constexpr int min_ctas() {
     return (!NATIVE && sizeof(ST) == 4) ? 6 : 7;
   }
 };
 
-// Dynamic shared memory of one verify CTA covering NS tiles, in bytes: the
-// mbarrier (16 bytes), the tile buffer the bulk copies fill (NS > 1 only),
-// then the staged keys, queries, values and gates (plus, for the
-// per-channel KDA gate, the window's [W][K] decay vectors).
-template <int K, typename ST>
-__host__ __device__ constexpr size_t verify_tile_bytes(int NS) {
-  return NS > 1 ? (size_t)VerifyTile<K>::VT * K * sizeof(ST) : 0;
-}
-template <int K, typename ST, bool KDA>
-__host__ __device__ constexpr size_t verify_smem_bytes(int W, int NS) {
-  return 16 + verify_tile_bytes<K, ST>(NS) +
-         sizeof(float) * (size_t)W * (2 * K + NS * VerifyTile<K>::VT + 4 + (KDA ? K : 0));
-}
+// Shared memory of one verify CTA covering NS tiles (SV = NS * VT staged
+// value rows), as float offsets after the mbarriers (kBarBytes) and the
+// nbuf tile buffers the bulk copies fill (NS > 1 only).
+constexpr int kMaxTileBufs = 4;
+constexpr int kBarBytes = 8 * kMaxTileBufs;
+template <int K, typename ST, bool KDA, bool NATIVE>
+struct VerifySmem {
+  int W, SV;
+  __host__ __device__ constexpr VerifySmem(int W_, int NS)
+      : W(W_), SV(NS * VerifyTile<K>::VT) {}
+  __host__ __device__ constexpr size_t tile_bytes(int NS) const {
+    return NS > 1 ? (size_t)VerifyTile<K>::VT * K * sizeof(ST) : 0;
+  }
+  __host__ __device__ constexpr int kt() const { return 0; }             // [W][K] gamma khat
+  __host__ __device__ constexpr int qt() const { return W * K; }         // [W][K] gamma qhat
+  __host__ __device__ constexpr int v() const { return 2 * W * K; }      // [W][SV] values
+  __host__ __device__ constexpr int gs() const { return v() + W * SV; }  // [W][4] alpha, beta
+  __host__ __device__ constexpr int ab() const { return gs() + 4 * W; }  // [2][W][W] A, B
+  // A and B padded to whole 16-byte pieces: al is read and written in them
+  __host__ __device__ constexpr int al() const { return ab() + ((2 * W * W + 3) & ~3); }  // [W][K] (KDA)
+  // khat and qhat ([W][K] each) are read only while the window is staged
+  // and, in the verify, share their space with the products C kt, C qt
+  // ([W][2][SV]) and u ([W][SV]), which are written only after it; the
+  // native kernel still folds with khat after its products, so there they
+  // are separate
+  __host__ __device__ constexpr int kh() const { return al() + (KDA ? W * K : 0); }
+  __host__ __device__ constexpr int qh() const { return kh() + W * K; }
+  __host__ __device__ constexpr int pq() const { return NATIVE ? qh() + W * K : kh(); }
+  __host__ __device__ constexpr int u() const { return pq() + 2 * W * SV; }
+  __host__ __device__ constexpr int floats() const {
+    return (u() + W * SV) > (qh() + W * K) ? (u() + W * SV) : (qh() + W * K);
+  }
+  __host__ __device__ constexpr size_t bytes(int NS, int nbuf) const {
+    return kBarBytes + nbuf * tile_bytes(NS) + sizeof(float) * (size_t)floats();
+  }
+};
 
 // A tile's checkpoint rows from the shared-memory tile buffer (a verbatim
 // copy of VT contiguous state rows) into the register buffer.
@@ -137,77 +148,64 @@ __device__ __forceinline__ void load_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], con
   }
 }
 
-// The draft window over one tile whose state is in s.  vt_off: this tile's
-// first row inside the CTA's staged value rows.  al_s: the window's
-// per-channel decay vectors [W][K] (KDA), unused for the scalar gate.
-template <int K, typename ST, bool NATIVE, bool FULL, bool KDA>
-__device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], const VerifyParams& p,
-                                         int tile, int h, int r, int w, long long t0, int vt_off,
-                                         int vrow_stride, const float* kh_s, const float* qh_s,
-                                         const float* v_s, const float* gs_s, const float* al_s,
-                                         int warp, int l, int lr) {
-  using Tile = VerifyTile<K>;
-  constexpr int LPR = Tile::LPR, RPW = Tile::RPW, RPT = Tile::RPT, VT = Tile::VT;
-  const size_t rec_base = ((size_t)r * p.HV + h) * p.W;
-  // the d half (lower LPR/2 lanes) and the o half of a row's lanes after
-  // the first exchange; the first o lane writes the row's outputs
-  const bool upper = LPR > 1 && (l & (LPR / 2)) != 0;
-  const int lane = lr * LPR + l;
-  const bool writer = (l == LPR / 2);
-  int rows[RPT];
-  float* optr[RPT];
-  float* uptr[RPT];
-  ST* sptr[RPT];
+// Recursive halving of N per-lane values over the lanes of a row group: at
+// lane distance OFF the lane with that bit set keeps the upper half of its
+// values and sends the lower half, its partner the reverse, and each adds
+// what it receives; with one value left the remaining distances are plain
+// butterfly additions.  base accumulates the index of the lane's first
+// remaining value.
+template <int OFF, int N>
+struct LaneHalve {
+  template <int NV>
+  static __device__ __forceinline__ void run(float (&x)[NV], int l, int& base) {
+    if constexpr (OFF >= 1) {
+      if constexpr (N > 1) {
+        constexpr int H = N / 2;
+        const bool up = (l & OFF) != 0;
 #pragma unroll
-  for (int g = 0; g < RPT; ++g) {
-    rows[g] = tile * VT + (g * Tile::WARPS + warp) * RPW + lr;
-    optr[g] = p.out + t0 * p.out_stride + (size_t)h * p.V + rows[g];
-    uptr[g] = NATIVE ? nullptr : p.rec_u + rec_base * p.V + rows[g];
-    sptr[g] = NATIVE ? static_cast<ST*>(p.snaps) + ((size_t)r * p.W * p.HV + h) * (size_t)p.V * K +
-                           (size_t)rows[g] * K + 4 * l
-                     : nullptr;
-  }
-  const size_t snap_step = (size_t)p.HV * p.V * K;
-  // ---- the draft window, token by token, state in registers.  In VERIFY
-  // ---- mode the state after the last token is never read: that token runs
-  // ---- without the update.
-  auto token = [&](int t, auto update_tag) {
-    constexpr bool UPDATE = decltype(update_tag)::value;
-    const ulonglong2 gq = *reinterpret_cast<const ulonglong2*>(gs_s + 4 * t);
-    [[maybe_unused]] const f32x2 al2 = gq.x;  // (alpha, alpha); unused with the KDA decay
-    const float2 bk = unpack2(gq.y);
-    const float be = bk.x, kq = bk.y;
-    if constexpr (KDA) {
-      // H = S diag(alpha): each pair of this thread's columns by its own
-      // gates, applied before the keys and queries are loaded so that the
-      // gate registers are free again
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const ulonglong2 a4 = *reinterpret_cast<const ulonglong2*>(al_s + t * K + 4 * (l + LPR * m));
-#pragma unroll
-        for (int g = 0; g < RPT; ++g) {
-          s[g][2 * m] = mul2(s[g][2 * m], a4.x);
-          s[g][2 * m + 1] = mul2(s[g][2 * m + 1], a4.y);
+        for (int i = 0; i < H; ++i) {
+          const float send = up ? x[i] : x[i + H];
+          const float keep = up ? x[i + H] : x[i];
+          x[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, OFF));
         }
+        if (up) base += H;
+        LaneHalve<OFF / 2, H>::run(x, l, base);
+      } else {
+        x[0] = __fadd_rn(x[0], __shfl_xor_sync(0xffffffffu, x[0], OFF));
+        LaneHalve<OFF / 2, 1>::run(x, l, base);
       }
     }
+  }
+};
+
+// Per token: the tile's rows against kt_t and qt_t, summed over each row's
+// lanes, into pq_s[t][0 / 1][row0 + row].  Value v = 2 g + which of a lane
+// is row group g's C kt (which 0) or C qt (which 1).
+template <int K>
+__device__ __forceinline__ void tile_products(const f32x2 (&s)[VerifyTile<K>::RPT][8],
+                                              const float* kt_s, const float* qt_s, float* pq_s,
+                                              int w, int SV, int row0, int warp, int l, int lr) {
+  using Tile = VerifyTile<K>;
+  constexpr int LPR = Tile::LPR, RPW = Tile::RPW, RPT = Tile::RPT;
+  constexpr int NV = 2 * RPT;                       // values per lane
+  constexpr int NSTEP = LPR < NV ? LPR : NV;        // lanes the halving spans
+  constexpr int NR = NV / NSTEP;                    // values left per lane
+  constexpr int DUP = LPR / NSTEP - 1;              // lane bits holding copies
+#pragma unroll 1
+  for (int t = 0; t < w; ++t) {
     f32x2 kk[8], qq[8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kh_s + t * K + 4 * (l + LPR * m));
-      const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(qh_s + t * K + 4 * (l + LPR * m));
+      const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kt_s + t * K + 4 * (l + LPR * m));
+      const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(qt_s + t * K + 4 * (l + LPR * m));
       kk[2 * m] = k4.x; kk[2 * m + 1] = k4.y;
       qq[2 * m] = q4.x; qq[2 * m + 1] = q4.y;
     }
+    float x[NV];
 #pragma unroll
     for (int g = 0; g < RPT; ++g) {
-      // H = alpha * S (the per-channel decay was applied above)
-      if constexpr (!KDA) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s[g][j] = mul2(s[g][j], al2);
-      }
-      // d = H khat and H qhat in one pass: pair accumulators over pairs
-      // 0-3 and 4-7, combined pairwise, lanes summed, then the LPR lanes
+      // pair accumulators over pairs 0-3 and 4-7, combined pairwise, then
+      // the two lanes of the pair
       f32x2 da = mul2(s[g][0], kk[0]), db = mul2(s[g][4], kk[4]);
       f32x2 oa = mul2(s[g][0], qq[0]), ob = mul2(s[g][4], qq[4]);
 #pragma unroll
@@ -218,61 +216,33 @@ __device__ __forceinline__ void run_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], cons
         ob = fma2(s[g][4 + j], qq[4 + j], ob);
       }
       const float2 dd = unpack2(add2(da, db)), oo = unpack2(add2(oa, ob));
-      float d = __fadd_rn(dd.x, dd.y), o = __fadd_rn(oo.x, oo.y);
-      if (LPR > 1) {
-        // halving exchange: the d half keeps d and sends o, the o half the
-        // reverse; then each half sums its own value over its lanes
-        const float keep = upper ? o : d, send = upper ? d : o;
-        float x = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, LPR / 2));
-#pragma unroll
-        for (int off = LPR / 4; off >= 1; off >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
-        d = __shfl_sync(0xffffffffu, x, lane - l);  // every lane takes d from the row's first lane
-        o = x;                                      // meaningful on the o half
-      }
-      const float vi = (FULL || rows[g] < p.V) ? v_s[t * vrow_stride + vt_off + rows[g] - tile * VT] : 0.f;
-      const float u = __fmul_rn(be, __fsub_rn(vi, d));
-      o = __fmaf_rn(u, kq, o);
-      // S = H + u khat^T
-      if (UPDATE) {
-        const f32x2 u2 = pack2(u, u);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s[g][j] = fma2(u2, kk[j], s[g][j]);
-      }
-      if (FULL || rows[g] < p.V) {
-        if (writer) {
-          *optr[g] = o;
-          if (!NATIVE) *uptr[g] = u;
-        }
-        if (NATIVE) {
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            store_state_pairs(sptr[g] + 4 * LPR * m, s[g][2 * m], s[g][2 * m + 1]);
-        }
-      }
-      optr[g] += p.out_stride;
-      if (!NATIVE) uptr[g] += p.V;
-      if (NATIVE) sptr[g] += snap_step;
+      x[2 * g] = __fadd_rn(dd.x, dd.y);
+      x[2 * g + 1] = __fadd_rn(oo.x, oo.y);
     }
-  };
-  if constexpr (NATIVE) {
-    for (int t = 0; t < w; ++t) token(t, std::true_type{});
-  } else {
-    for (int t = 0; t + 1 < w; ++t) token(t, std::true_type{});
-    token(w - 1, std::false_type{});
+    int base = 0;
+    LaneHalve<LPR / 2, NV>::run(x, l, base);
+    if ((l & DUP) == 0) {
+#pragma unroll
+      for (int i = 0; i < NR; ++i) {
+        const int v = base + i, g = v >> 1, which = v & 1;
+        pq_s[(2 * t + which) * SV + row0 + (g * Tile::WARPS + warp) * RPW + lr] = x[i];
+      }
+    }
   }
 }
 
 // One CTA runs NS consecutive tiles of one (request row, value head): the
-// window's keys, queries, gates and values are staged once for all of them,
-// then each tile's checkpoint rows are loaded and its window run in turn.
+// window's side is staged once for all of them, each tile's products with
+// it are formed in turn, then each row's u_t and o_t.
 template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS, bool KDA>
 __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
                                   VerifyTile<K>::template min_ctas<NATIVE, ST, KDA>())
-    gdn_verify_kernel(const VerifyParams p) {
+    gdn_verify_kernel(const VerifyParams p, int nbuf) {
   using Tile = VerifyTile<K>;
   constexpr int LPR = Tile::LPR, RPT = Tile::RPT, VT = Tile::VT;
   constexpr bool BULK = NS > 1;  // tiles arrive by bulk copies into shared memory
   static_assert(!BULK || FULL, "bulk-copied tiles are whole tiles");
+  static_assert(!NATIVE || NS == 1, "the native form runs one tile per CTA");
   extern __shared__ __align__(16) unsigned char smem_raw[];
 
   const int span = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
@@ -304,37 +274,45 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   const int l = lane % LPR;   // column lane inside the row group
   const int lr = lane / LPR;  // row inside the warp's row group
 
-  // ---- the first tile's checkpoint loads go out first; they stay in flight
-  // ---- while the window's inputs are staged.  Row group g holds columns
+  // ---- the first tiles' checkpoint loads go out first; they stay in flight
+  // ---- while the window is staged.  Row group g holds columns
   // ---- 4*(l + LPR*m) + {0..3}: s[g][2m] = +0,+1 and s[g][2m+1] = +2,+3.
   const ST* S0 = static_cast<const ST*>(p.pool) + ((size_t)src.slot * p.HV + h) * (size_t)p.V * K;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
-  ST* tbuf = reinterpret_cast<ST*>(smem_raw + 16);
-  constexpr uint32_t kTileBytes = (uint32_t)verify_tile_bytes<K, ST>(NS);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);  // one per tile buffer
+  ST* tbuf = reinterpret_cast<ST*>(smem_raw + kBarBytes);
+  const VerifySmem<K, ST, KDA, NATIVE> lay(p.W, NS);
+  constexpr uint32_t kTileBytes = BULK ? (uint32_t)(VT * K * sizeof(ST)) : 0u;
+  constexpr int kTileElems = BULK ? VT * K : 0;
   f32x2 s[RPT][8];
   if constexpr (BULK) {
-    // one thread requests the first tile as a single bulk copy
+    // one thread requests the first nbuf tiles, one bulk copy each
     if (tid == 0) {
-      mbar_init(bar, 1);
-      mbar_expect_tx(bar, kTileBytes);
-      bulk_load(tbuf, S0 + (size_t)tile0 * VT * K, kTileBytes, bar);
+      for (int b = 0; b < nbuf; ++b) mbar_init(bar + b, 1);
+      for (int b = 0; b < nbuf; ++b) {
+        mbar_expect_tx(bar + b, kTileBytes);
+        bulk_load(tbuf + b * kTileElems, S0 + (size_t)(tile0 + b) * VT * K, kTileBytes, bar + b);
+      }
     }
   } else {
     load_tile<K, ST, FULL>(s, S0, tile0, p.V, warp, l, lr);
   }
 
-  // ---- stage normalised keys / queries, their dot product, the gates and
-  // ---- the value rows of all NS tiles for the whole window in shared
-  // ---- memory.  Every global load of the stage is issued before any of its
+  // ---- stage the window: normalised keys and queries, gates, values.
+  // ---- Every global load of the stage is issued before any of its
   // ---- arithmetic or shared-memory stores, so the stage costs one memory
-  // ---- round trip after the row plan's instead of one per loop pass (a
-  // ---- load is not moved above an earlier pass's stores by the compiler).
-  constexpr int SV = NS * VT;           // staged value rows
-  float* kh_s = reinterpret_cast<float*>(smem_raw + 16 + kTileBytes);  // [W][K]
-  float* qh_s = kh_s + p.W * K;         // [W][K]
-  float* v_s = qh_s + p.W * K;          // [W][SV]
-  float* gs_s = v_s + p.W * SV;         // [W][4]: alpha, alpha, beta, khat . qhat
-  float* al_s = gs_s + 4 * p.W;         // [W][K]: per-channel decay (KDA only)
+  // ---- round trip after the row plan's instead of one per loop pass.
+  constexpr int SV = NS * VT;  // staged value rows
+  float* sm = reinterpret_cast<float*>(smem_raw + kBarBytes + (size_t)nbuf * kTileBytes);
+  float* kh_s = sm + lay.kh();
+  float* qh_s = sm + lay.qh();
+  float* kt_s = sm + lay.kt();
+  float* qt_s = sm + lay.qt();
+  float* v_s = sm + lay.v();
+  float* pq_s = sm + lay.pq();
+  float* u_s = sm + lay.u();
+  float* gs_s = sm + lay.gs();
+  float* ab_s = sm + lay.ab();
+  float* al_s = sm + lay.al();
   const QKV* qb = static_cast<const QKV*>(p.q);
   const QKV* kb = static_cast<const QKV*>(p.k);
   const QKV* vb = static_cast<const QKV*>(p.v);
@@ -415,32 +393,20 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
       // x / sqrt(|x|^2 + eps) as x * rsqrt(|x|^2 + eps), rsqrt correctly rounded
       const float kr = __frsqrt_rn(__fadd_rn(ks, kL2NormEps));
       const float qr = __frsqrt_rn(__fadd_rn(qs, kL2NormEps));
-      float kn[4], qn[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kn[e] = __fmul_rn(kx[j][e], kr);
-        qn[e] = __fmul_rn(qx[j][e], qr);
-      }
-      float kq = __fmul_rn(kn[0], qn[0]);
-#pragma unroll
-      for (int e = 1; e < 4; ++e) kq = __fmaf_rn(kn[e], qn[e], kq);
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) kq = __fadd_rn(kq, __shfl_xor_sync(0xffffffffu, kq, off));
       if (lane < K / 4) {
-        *reinterpret_cast<float4*>(kh_s + t * K + 4 * lane) = make_float4(kn[0], kn[1], kn[2], kn[3]);
-        *reinterpret_cast<float4*>(qh_s + t * K + 4 * lane) = make_float4(qn[0], qn[1], qn[2], qn[3]);
+        *reinterpret_cast<float4*>(kh_s + t * K + 4 * lane) =
+            make_float4(__fmul_rn(kx[j][0], kr), __fmul_rn(kx[j][1], kr), __fmul_rn(kx[j][2], kr),
+                        __fmul_rn(kx[j][3], kr));
+        *reinterpret_cast<float4*>(qh_s + t * K + 4 * lane) =
+            make_float4(__fmul_rn(qx[j][0], qr), __fmul_rn(qx[j][1], qr), __fmul_rn(qx[j][2], qr),
+                        __fmul_rn(qx[j][3], qr));
       }
-      if (lane == 0) gs_s[4 * t + 3] = kq;
     }
   }
-  // gates
+  // gates: [W][4] = alpha, beta, -, -
   if (glane) {
-    if constexpr (!KDA) {
-      const float al = gate_decay(g_a, g_Alog, g_dt);
-      gs_s[4 * lane] = al;
-      gs_s[4 * lane + 1] = al;
-    }
-    gs_s[4 * lane + 2] = gate_beta(g_b);
+    if constexpr (!KDA) gs_s[4 * lane] = gate_decay(g_a, g_Alog, g_dt);
+    gs_s[4 * lane + 1] = gate_beta(g_b);
   }
   if constexpr (KDA) {
     const float A = expf(kAlog);  // once per head, not per channel
@@ -485,6 +451,70 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   }
   __syncthreads();
 
+  // ---- the window's side.  Channel c: gamma_t = gamma_{t-1} * alpha_t,
+  // ---- kt_t = gamma_t khat_t, qt_t = gamma_t qhat_t (one thread per
+  // ---- channel, K <= 128 threads).
+  auto decay_of = [&](int t, int c) { return KDA ? al_s[t * K + c] : gs_s[4 * t]; };
+  for (int c = tid; c < K; c += Tile::THREADS) {
+    float gam = 1.f;
+    for (int t = 0; t < w; ++t) {
+      gam = __fmul_rn(gam, decay_of(t, c));
+      kt_s[t * K + c] = __fmul_rn(gam, kh_s[t * K + c]);
+      qt_s[t * K + c] = __fmul_rn(gam, qh_s[t * K + c]);
+    }
+  }
+  // A_{t,j} = <rho_{t,j} khat_j, khat_t> (j < t) and B_{t,j} = <rho_{t,j}
+  // khat_j, qhat_t> (j <= t): warp j (mod 4) walks t upward from j with the
+  // running product rho per channel, each lane summing its channels c =
+  // lane + 32 i in order; four tokens' eight sums at a time are then summed
+  // over the warp's lanes by recursive halving (one chain of five exchanges
+  // for all eight).
+  float* A_s = ab_s;
+  float* B_s = ab_s + p.W * p.W;
+  constexpr int CPL = (K + 31) / 32;  // channels per lane
+  for (int j = warp; j < w; j += Tile::WARPS) {
+    float kr[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      kr[i] = c < K ? kh_s[j * K + c] : 0.f;  // rho_{j,j} khat_j = khat_j
+    }
+    for (int tb = j; tb < w; tb += 4) {
+      float x[8];
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) {
+        const int t = tb + tt;
+        float sa = 0.f, sb = 0.f;
+        if (t < w) {
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = lane + 32 * i;
+            if (c < K) {
+              if (t > j) kr[i] = __fmul_rn(kr[i], decay_of(t, c));
+              sa = __fmaf_rn(kr[i], kh_s[t * K + c], sa);
+              sb = __fmaf_rn(kr[i], qh_s[t * K + c], sb);
+            }
+          }
+        }
+        x[2 * tt] = sa;
+        x[2 * tt + 1] = sb;
+      }
+      int base = 0;
+      LaneHalve<16, 8>::run(x, lane, base);  // one sum per lane, equal within groups of 4
+      if ((lane & 3) == 0) {
+        const int t = tb + (base >> 1);
+        if (t < w) {
+          if ((base & 1) == 0) {
+            if (t > j) A_s[t * p.W + j] = x[0];
+          } else {
+            B_s[t * p.W + j] = x[0];
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+
   const size_t rec_base = ((size_t)r * p.HV + h) * p.W;  // record position 0
   if (!NATIVE && span == 0) {
     // records are 16-byte aligned and K is a multiple of 4
@@ -497,43 +527,110 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
       if (tid < w) p.rec_g[rec_base + tid] = gs_s[4 * tid];
     }
   }
+  // the products below overwrite khat and qhat in the verify: with bulk
+  // copies the tile loop's first barrier orders them after these reads
+  if constexpr (!NATIVE && !BULK) __syncthreads();
 
-  // ---- the tiles one after another.  With bulk copies, tile i + 1 is
-  // ---- requested into the (single) shared buffer as soon as every warp has
-  // ---- moved tile i into registers, so it streams in while tile i runs.
+  // ---- the tiles one after another: C kt_t and C qt_t of every row.  With
+  // ---- bulk copies, tile i sits in buffer i % nbuf, and tile i + nbuf is
+  // ---- requested into it as soon as every warp has moved tile i into
+  // ---- registers.
 #pragma unroll 1
   for (int i = 0; i < NS; ++i) {
     if constexpr (BULK) {
-      const bool ok = mbar_wait(bar, i & 1);
-      if (ok) load_tile_shared<K>(s, tbuf, warp, l, lr);
+      const int b = i % nbuf;
+      const uint32_t par = (uint32_t)(i / nbuf) & 1u;
+      const bool ok = mbar_wait(bar + b, par);
+      if (ok) load_tile_shared<K>(s, tbuf + b * kTileElems, warp, l, lr);
       if (__syncthreads_or(!ok)) {
-        // never expected: report, let the copy in flight land, and stop
+        // never expected: report, let the copies in flight land, and stop
         if (tid == 0 && p.err) atomicOr(p.err, GDN_ROW_ERR_TIMEOUT);
-        mbar_wait(bar, i & 1);
+        for (int j = i; j < NS && j < i + nbuf; ++j) mbar_wait(bar + j % nbuf, (uint32_t)(j / nbuf) & 1u);
         return;
       }
-      if (tid == 0 && i + 1 < NS) {
+      if (tid == 0 && i + nbuf < NS) {
         fence_proxy_async_shared();
-        mbar_expect_tx(bar, kTileBytes);
-        bulk_load(tbuf, S0 + (size_t)(tile0 + i + 1) * VT * K, kTileBytes, bar);
+        mbar_expect_tx(bar + b, kTileBytes);
+        bulk_load(tbuf + b * kTileElems, S0 + (size_t)(tile0 + i + nbuf) * VT * K, kTileBytes,
+                  bar + b);
       }
     } else {
       if (i > 0) load_tile<K, ST, FULL>(s, S0, tile0 + i, p.V, warp, l, lr);
     }
-    run_tile<K, ST, NATIVE, FULL, KDA>(s, p, tile0 + i, h, r, w, t0, i * VT, SV, kh_s, qh_s, v_s,
-                                       gs_s, al_s, warp, l, lr);
+    tile_products<K>(s, kt_s, qt_s, pq_s, w, SV, i * VT, warp, l, lr);
+  }
+  __syncthreads();
+
+  // ---- u_t and o_t, one thread per row: d = C kt + sum_{j<t} A u_j,
+  // ---- u = beta (v - d), o = C qt + sum_{j<=t} B u_j
+  for (int row = tid; row < SV; row += Tile::THREADS) {
+    const int hrow = tile0 * VT + row;  // row of the head
+    if (!FULL && hrow >= p.V) continue;
+    float* optr = p.out + t0 * p.out_stride + (size_t)h * p.V + hrow;
+    for (int t = 0; t < w; ++t) {
+      float d = pq_s[(2 * t) * SV + row];
+      for (int j = 0; j < t; ++j) d = __fmaf_rn(A_s[t * p.W + j], u_s[j * SV + row], d);
+      const float u = __fmul_rn(gs_s[4 * t + 1], __fsub_rn(v_s[t * SV + row], d));
+      float o = pq_s[(2 * t + 1) * SV + row];
+      for (int j = 0; j < t; ++j) o = __fmaf_rn(B_s[t * p.W + j], u_s[j * SV + row], o);
+      o = __fmaf_rn(B_s[t * p.W + t], u, o);
+      u_s[t * SV + row] = u;
+      optr[t * p.out_stride] = o;
+      if (!NATIVE) p.rec_u[(rec_base + t) * p.V + hrow] = u;
+    }
+  }
+
+  // ---- native baseline: fold the tile token by token with the commit's
+  // ---- update and write the state after every token
+  if constexpr (NATIVE) {
+    __syncthreads();
+    const size_t snap_step = (size_t)p.HV * p.V * K;
+    ST* sbase = static_cast<ST*>(p.snaps) + ((size_t)r * p.W * p.HV + h) * (size_t)p.V * K;
+    for (int t = 0; t < w; ++t) {
+      f32x2 kk[8], al2[8];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(kh_s + t * K + 4 * (l + LPR * m));
+        kk[2 * m] = k4.x; kk[2 * m + 1] = k4.y;
+        if constexpr (KDA) {
+          const ulonglong2 a4 = *reinterpret_cast<const ulonglong2*>(al_s + t * K + 4 * (l + LPR * m));
+          al2[2 * m] = a4.x; al2[2 * m + 1] = a4.y;
+        } else {
+          al2[2 * m] = al2[2 * m + 1] = pack2(gs_s[4 * t], gs_s[4 * t]);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < RPT; ++g) {
+        const int tr = (g * Tile::WARPS + warp) * Tile::RPW + lr;  // row in the tile
+        const int hrow = tile0 * VT + tr;
+        const float u = u_s[t * SV + tr];
+        const f32x2 u2 = pack2(u, u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[g][j] = fold2(s[g][j], al2[j], u2, kk[j]);
+        if (FULL || hrow < p.V) {
+          ST* dst = sbase + t * snap_step + (size_t)hrow * K + 4 * l;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) store_state_pairs(dst + 4 * LPR * m, s[g][2 * m], s[g][2 * m + 1]);
+        }
+      }
+    }
   }
 }
+
+#ifndef GDN_NB_DEFAULT
+#define GDN_NB_DEFAULT 1
+#endif
 
 template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS, bool KDA>
 static void launch_tiles(const VerifyParams& p, int ntiles, cudaStream_t stream) {
   using Tile = VerifyTile<K>;
   dim3 grid(ntiles / NS, p.HV, p.batch);
-  const size_t smem = verify_smem_bytes<K, ST, KDA>(p.W, NS);
+  const int nbuf = NS > 1 ? (GDN_NB_DEFAULT < NS ? GDN_NB_DEFAULT : NS) : 1;
+  const size_t smem = VerifySmem<K, ST, KDA, NATIVE>(p.W, NS).bytes(NS, nbuf);
   auto kern = gdn_verify_kernel<K, QKV, ST, NATIVE, FULL, NS, KDA>;
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  kern<<<grid, Tile::THREADS, smem, stream>>>(p);
+  kern<<<grid, Tile::THREADS, smem, stream>>>(p, nbuf);
 }
 
 // The verify runs 4 (else 2) tiles of a head per CTA when they divide the
