@@ -60,10 +60,11 @@ struct VerifyTile {
 };
 
 // Shared memory of one verify CTA covering NS tiles (SV = NS * VT staged
-// value rows), as float offsets after the mbarriers (kBarBytes) and the
-// nbuf tile buffers the bulk copies fill (NS > 1 only).
-constexpr int kMaxTileBufs = 4;
-constexpr int kBarBytes = 8 * kMaxTileBufs;
+// value rows), as float offsets after the mbarrier (kBarBytes) and the tile
+// buffer the bulk copies fill (NS > 1 only).  One buffer: two to four,
+// each CTA streaming more tiles, measured slower on every workload (the
+// shared memory they take costs resident CTAs).
+constexpr int kBarBytes = 16;
 template <int K, typename ST, bool KDA, bool NATIVE>
 struct VerifySmem {
   int W, SV;
@@ -91,8 +92,8 @@ struct VerifySmem {
   __host__ __device__ constexpr int floats() const {
     return (u() + W * SV) > (qh() + W * K) ? (u() + W * SV) : (qh() + W * K);
   }
-  __host__ __device__ constexpr size_t bytes(int NS, int nbuf) const {
-    return kBarBytes + nbuf * tile_bytes(NS) + sizeof(float) * (size_t)floats();
+  __host__ __device__ constexpr size_t bytes(int NS) const {
+    return kBarBytes + tile_bytes(NS) + sizeof(float) * (size_t)floats();
   }
 };
 
@@ -148,6 +149,34 @@ __device__ __forceinline__ void load_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], con
   }
 }
 
+// One token's key and query L2-normalised by a whole warp: lane i < K / 4
+// holds elements 4 i .. 4 i + 3 of each (zeros elsewhere) and writes its
+// four normalised values into khat_row and qhat_row.
+template <int K>
+__device__ __forceinline__ void normalise_token(const float (&kx)[4], const float (&qx)[4],
+                                                float* khat_row, float* qhat_row, int lane) {
+  float ks = __fmul_rn(kx[0], kx[0]), qs = __fmul_rn(qx[0], qx[0]);
+#pragma unroll
+  for (int e = 1; e < 4; ++e) {
+    ks = __fmaf_rn(kx[e], kx[e], ks);
+    qs = __fmaf_rn(qx[e], qx[e], qs);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    ks = __fadd_rn(ks, __shfl_xor_sync(0xffffffffu, ks, off));
+    qs = __fadd_rn(qs, __shfl_xor_sync(0xffffffffu, qs, off));
+  }
+  // x / sqrt(|x|^2 + eps) as x * rsqrt(|x|^2 + eps), rsqrt correctly rounded
+  const float kr = __frsqrt_rn(__fadd_rn(ks, kL2NormEps));
+  const float qr = __frsqrt_rn(__fadd_rn(qs, kL2NormEps));
+  if (lane < K / 4) {
+    *reinterpret_cast<float4*>(khat_row + 4 * lane) = make_float4(
+        __fmul_rn(kx[0], kr), __fmul_rn(kx[1], kr), __fmul_rn(kx[2], kr), __fmul_rn(kx[3], kr));
+    *reinterpret_cast<float4*>(qhat_row + 4 * lane) = make_float4(
+        __fmul_rn(qx[0], qr), __fmul_rn(qx[1], qr), __fmul_rn(qx[2], qr), __fmul_rn(qx[3], qr));
+  }
+}
+
 // Recursive halving of N per-lane values over the lanes of a row group: at
 // lane distance OFF the lane with that bit set keeps the upper half of its
 // values and sends the lower half, its partner the reverse, and each adds
@@ -178,10 +207,127 @@ struct LaneHalve {
   }
 };
 
+// The window's side, from khat, qhat ([W][K]) and the gates (gs [W][4]
+// alpha, beta; al [W][K] per channel with the KDA decay), by `nthreads`
+// threads (`nwarps` whole warps):
+//   channel c: gamma_t = gamma_{t-1} * alpha_t, kt_t = gamma_t khat_t,
+//   qt_t = gamma_t qhat_t (one thread per channel);
+//   A_{t,j} = <rho_{t,j} khat_j, khat_t> (j < t), B_{t,j} = <rho_{t,j}
+//   khat_j, qhat_t> (j <= t): warp j (mod nwarps) walks t upward from j with
+//   the running product rho per channel, each lane summing its channels
+//   c = lane + 32 i in order; four tokens' eight sums at a time are then
+//   summed over the warp's lanes by recursive halving (one chain of five
+//   exchanges for all eight).
+// The caller orders the inputs before and the outputs after (barriers).
+template <int K, bool KDA>
+__device__ __forceinline__ void window_side(int w, int W, const float* kh_s, const float* qh_s,
+                                            const float* gs_s, const float* al_s, float* kt_s,
+                                            float* qt_s, float* A_s, float* B_s, int tid,
+                                            int nthreads, int warp, int nwarps, int lane) {
+  auto decay_of = [&](int t, int c) { return KDA ? al_s[t * K + c] : gs_s[4 * t]; };
+  for (int c = tid; c < K; c += nthreads) {
+    float gam = 1.f;
+    for (int t = 0; t < w; ++t) {
+      gam = __fmul_rn(gam, decay_of(t, c));
+      kt_s[t * K + c] = __fmul_rn(gam, kh_s[t * K + c]);
+      qt_s[t * K + c] = __fmul_rn(gam, qh_s[t * K + c]);
+    }
+  }
+  constexpr int CPL = (K + 31) / 32;  // channels per lane
+  for (int j = warp; j < w; j += nwarps) {
+    float kr[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      kr[i] = c < K ? kh_s[j * K + c] : 0.f;  // rho_{j,j} khat_j = khat_j
+    }
+    for (int tb = j; tb < w; tb += 4) {
+      float x[8];
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) {
+        const int t = tb + tt;
+        float sa = 0.f, sb = 0.f;
+        if (t < w) {
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = lane + 32 * i;
+            if (c < K) {
+              if (t > j) kr[i] = __fmul_rn(kr[i], decay_of(t, c));
+              sa = __fmaf_rn(kr[i], kh_s[t * K + c], sa);
+              sb = __fmaf_rn(kr[i], qh_s[t * K + c], sb);
+            }
+          }
+        }
+        x[2 * tt] = sa;
+        x[2 * tt + 1] = sb;
+      }
+      int base = 0;
+      LaneHalve<16, 8>::run(x, lane, base);  // one sum per lane, equal within groups of 4
+      if ((lane & 3) == 0) {
+        const int t = tb + (base >> 1);
+        if (t < w) {
+          if ((base & 1) == 0) {
+            if (t > j) A_s[t * W + j] = x[0];
+          } else {
+            B_s[t * W + j] = x[0];
+          }
+        }
+      }
+    }
+  }
+}
+
+// u_t and o_t of one row from its products pq ([W][2][SV], row `row`), its
+// values vload(t) and the window's beta (gs) and A, B ([W][W]):
+//   d = C kt + sum_{j<t} A u_j,  u = beta (v - d),  o = C qt + sum_{j<=t} B u_j.
+// u_t lands in u_s[t][row]; o_t at optr[t * out_stride]; u_t also at
+// uptr[t * V] when uptr is not null.  WC > 0: the record stride W is WC
+// and the loops are unrolled, u_j kept in registers (the same operations in
+// the same order).
+template <int WC, typename VLoad>
+__device__ __forceinline__ void row_recurrence(int row, int w, int W, int SV, const float* pq_s,
+                                               float* u_s, const float* gs_s, const float* A_s,
+                                               const float* B_s, VLoad vload, float* optr,
+                                               long long out_stride, float* uptr, int V) {
+  if constexpr (WC > 0) {
+    float ur[WC];
+#pragma unroll
+    for (int t = 0; t < WC; ++t) {
+      if (t < w) {
+        float d = pq_s[(2 * t) * SV + row];
+#pragma unroll
+        for (int j = 0; j < t; ++j) d = __fmaf_rn(A_s[t * WC + j], ur[j], d);
+        const float u = __fmul_rn(gs_s[4 * t + 1], __fsub_rn(vload(t), d));
+        float o = pq_s[(2 * t + 1) * SV + row];
+#pragma unroll
+        for (int j = 0; j < t; ++j) o = __fmaf_rn(B_s[t * WC + j], ur[j], o);
+        o = __fmaf_rn(B_s[t * WC + t], u, o);
+        ur[t] = u;
+        u_s[t * SV + row] = u;
+        optr[t * out_stride] = o;
+        if (uptr) uptr[(size_t)t * V] = u;
+      }
+    }
+    return;
+  }
+  for (int t = 0; t < w; ++t) {
+    float d = pq_s[(2 * t) * SV + row];
+    for (int j = 0; j < t; ++j) d = __fmaf_rn(A_s[t * W + j], u_s[j * SV + row], d);
+    const float u = __fmul_rn(gs_s[4 * t + 1], __fsub_rn(vload(t), d));
+    float o = pq_s[(2 * t + 1) * SV + row];
+    for (int j = 0; j < t; ++j) o = __fmaf_rn(B_s[t * W + j], u_s[j * SV + row], o);
+    o = __fmaf_rn(B_s[t * W + t], u, o);
+    u_s[t * SV + row] = u;
+    optr[t * out_stride] = o;
+    if (uptr) uptr[(size_t)t * V] = u;
+  }
+}
+
 // Per token: the tile's rows against kt_t and qt_t, summed over each row's
 // lanes, into pq_s[t][0 / 1][row0 + row].  Value v = 2 g + which of a lane
-// is row group g's C kt (which 0) or C qt (which 1).
-template <int K>
+// is row group g's C kt (which 0) or C qt (which 1).  WC > 0: at most WC
+// tokens, the token loop unrolled.
+template <int K, int WC>
 __device__ __forceinline__ void tile_products(const f32x2 (&s)[VerifyTile<K>::RPT][8],
                                               const float* kt_s, const float* qt_s, float* pq_s,
                                               int w, int SV, int row0, int warp, int l, int lr) {
@@ -191,8 +337,7 @@ __device__ __forceinline__ void tile_products(const f32x2 (&s)[VerifyTile<K>::RP
   constexpr int NSTEP = LPR < NV ? LPR : NV;        // lanes the halving spans
   constexpr int NR = NV / NSTEP;                    // values left per lane
   constexpr int DUP = LPR / NSTEP - 1;              // lane bits holding copies
-#pragma unroll 1
-  for (int t = 0; t < w; ++t) {
+  auto token = [&](int t) {
     f32x2 kk[8], qq[8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -228,16 +373,24 @@ __device__ __forceinline__ void tile_products(const f32x2 (&s)[VerifyTile<K>::RP
         pq_s[(2 * t + which) * SV + row0 + (g * Tile::WARPS + warp) * RPW + lr] = x[i];
       }
     }
+  };
+  if constexpr (WC > 0) {
+#pragma unroll
+    for (int t = 0; t < WC; ++t)
+      if (t < w) token(t);
+  } else {
+#pragma unroll 1
+    for (int t = 0; t < w; ++t) token(t);
   }
 }
 
 // One CTA runs NS consecutive tiles of one (request row, value head): the
 // window's side is staged once for all of them, each tile's products with
 // it are formed in turn, then each row's u_t and o_t.
-template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS, bool KDA>
+template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS, bool KDA, int WC>
 __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
                                   VerifyTile<K>::template min_ctas<NATIVE, ST, KDA>())
-    gdn_verify_kernel(const VerifyParams p, int nbuf) {
+    gdn_verify_kernel(const VerifyParams p) {
   using Tile = VerifyTile<K>;
   constexpr int LPR = Tile::LPR, RPT = Tile::RPT, VT = Tile::VT;
   constexpr bool BULK = NS > 1;  // tiles arrive by bulk copies into shared memory
@@ -274,24 +427,21 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   const int l = lane % LPR;   // column lane inside the row group
   const int lr = lane / LPR;  // row inside the warp's row group
 
-  // ---- the first tiles' checkpoint loads go out first; they stay in flight
+  // ---- the first tile's checkpoint loads go out first; they stay in flight
   // ---- while the window is staged.  Row group g holds columns
   // ---- 4*(l + LPR*m) + {0..3}: s[g][2m] = +0,+1 and s[g][2m+1] = +2,+3.
   const ST* S0 = static_cast<const ST*>(p.pool) + ((size_t)src.slot * p.HV + h) * (size_t)p.V * K;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);  // one per tile buffer
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
   ST* tbuf = reinterpret_cast<ST*>(smem_raw + kBarBytes);
   const VerifySmem<K, ST, KDA, NATIVE> lay(p.W, NS);
   constexpr uint32_t kTileBytes = BULK ? (uint32_t)(VT * K * sizeof(ST)) : 0u;
-  constexpr int kTileElems = BULK ? VT * K : 0;
   f32x2 s[RPT][8];
   if constexpr (BULK) {
-    // one thread requests the first nbuf tiles, one bulk copy each
+    // one thread requests the first tile as a single bulk copy
     if (tid == 0) {
-      for (int b = 0; b < nbuf; ++b) mbar_init(bar + b, 1);
-      for (int b = 0; b < nbuf; ++b) {
-        mbar_expect_tx(bar + b, kTileBytes);
-        bulk_load(tbuf + b * kTileElems, S0 + (size_t)(tile0 + b) * VT * K, kTileBytes, bar + b);
-      }
+      mbar_init(bar, 1);
+      mbar_expect_tx(bar, kTileBytes);
+      bulk_load(tbuf, S0 + (size_t)tile0 * VT * K, kTileBytes, bar);
     }
   } else {
     load_tile<K, ST, FULL>(s, S0, tile0, p.V, warp, l, lr);
@@ -302,7 +452,7 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   // ---- arithmetic or shared-memory stores, so the stage costs one memory
   // ---- round trip after the row plan's instead of one per loop pass.
   constexpr int SV = NS * VT;  // staged value rows
-  float* sm = reinterpret_cast<float*>(smem_raw + kBarBytes + (size_t)nbuf * kTileBytes);
+  float* sm = reinterpret_cast<float*>(smem_raw + kBarBytes + kTileBytes);
   float* kh_s = sm + lay.kh();
   float* qh_s = sm + lay.qh();
   float* kt_s = sm + lay.kt();
@@ -379,28 +529,7 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
     for (int j = 0; j < 2; ++j) {
       const int t = tb + warp + j * Tile::WARPS;
       if (t >= w) break;  // warp-uniform
-      float ks = __fmul_rn(kx[j][0], kx[j][0]), qs = __fmul_rn(qx[j][0], qx[j][0]);
-#pragma unroll
-      for (int e = 1; e < 4; ++e) {
-        ks = __fmaf_rn(kx[j][e], kx[j][e], ks);
-        qs = __fmaf_rn(qx[j][e], qx[j][e], qs);
-      }
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        ks = __fadd_rn(ks, __shfl_xor_sync(0xffffffffu, ks, off));
-        qs = __fadd_rn(qs, __shfl_xor_sync(0xffffffffu, qs, off));
-      }
-      // x / sqrt(|x|^2 + eps) as x * rsqrt(|x|^2 + eps), rsqrt correctly rounded
-      const float kr = __frsqrt_rn(__fadd_rn(ks, kL2NormEps));
-      const float qr = __frsqrt_rn(__fadd_rn(qs, kL2NormEps));
-      if (lane < K / 4) {
-        *reinterpret_cast<float4*>(kh_s + t * K + 4 * lane) =
-            make_float4(__fmul_rn(kx[j][0], kr), __fmul_rn(kx[j][1], kr), __fmul_rn(kx[j][2], kr),
-                        __fmul_rn(kx[j][3], kr));
-        *reinterpret_cast<float4*>(qh_s + t * K + 4 * lane) =
-            make_float4(__fmul_rn(qx[j][0], qr), __fmul_rn(qx[j][1], qr), __fmul_rn(qx[j][2], qr),
-                        __fmul_rn(qx[j][3], qr));
-      }
+      normalise_token<K>(kx[j], qx[j], kh_s + t * K, qh_s + t * K, lane);
     }
   }
   // gates: [W][4] = alpha, beta, -, -
@@ -451,68 +580,11 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   }
   __syncthreads();
 
-  // ---- the window's side.  Channel c: gamma_t = gamma_{t-1} * alpha_t,
-  // ---- kt_t = gamma_t khat_t, qt_t = gamma_t qhat_t (one thread per
-  // ---- channel, K <= 128 threads).
-  auto decay_of = [&](int t, int c) { return KDA ? al_s[t * K + c] : gs_s[4 * t]; };
-  for (int c = tid; c < K; c += Tile::THREADS) {
-    float gam = 1.f;
-    for (int t = 0; t < w; ++t) {
-      gam = __fmul_rn(gam, decay_of(t, c));
-      kt_s[t * K + c] = __fmul_rn(gam, kh_s[t * K + c]);
-      qt_s[t * K + c] = __fmul_rn(gam, qh_s[t * K + c]);
-    }
-  }
-  // A_{t,j} = <rho_{t,j} khat_j, khat_t> (j < t) and B_{t,j} = <rho_{t,j}
-  // khat_j, qhat_t> (j <= t): warp j (mod 4) walks t upward from j with the
-  // running product rho per channel, each lane summing its channels c =
-  // lane + 32 i in order; four tokens' eight sums at a time are then summed
-  // over the warp's lanes by recursive halving (one chain of five exchanges
-  // for all eight).
+  // ---- the window's side: kt, qt, A and B
   float* A_s = ab_s;
   float* B_s = ab_s + p.W * p.W;
-  constexpr int CPL = (K + 31) / 32;  // channels per lane
-  for (int j = warp; j < w; j += Tile::WARPS) {
-    float kr[CPL];
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-      const int c = lane + 32 * i;
-      kr[i] = c < K ? kh_s[j * K + c] : 0.f;  // rho_{j,j} khat_j = khat_j
-    }
-    for (int tb = j; tb < w; tb += 4) {
-      float x[8];
-#pragma unroll
-      for (int tt = 0; tt < 4; ++tt) {
-        const int t = tb + tt;
-        float sa = 0.f, sb = 0.f;
-        if (t < w) {
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) {
-            const int c = lane + 32 * i;
-            if (c < K) {
-              if (t > j) kr[i] = __fmul_rn(kr[i], decay_of(t, c));
-              sa = __fmaf_rn(kr[i], kh_s[t * K + c], sa);
-              sb = __fmaf_rn(kr[i], qh_s[t * K + c], sb);
-            }
-          }
-        }
-        x[2 * tt] = sa;
-        x[2 * tt + 1] = sb;
-      }
-      int base = 0;
-      LaneHalve<16, 8>::run(x, lane, base);  // one sum per lane, equal within groups of 4
-      if ((lane & 3) == 0) {
-        const int t = tb + (base >> 1);
-        if (t < w) {
-          if ((base & 1) == 0) {
-            if (t > j) A_s[t * p.W + j] = x[0];
-          } else {
-            B_s[t * p.W + j] = x[0];
-          }
-        }
-      }
-    }
-  }
+  window_side<K, KDA>(w, p.W, kh_s, qh_s, gs_s, al_s, kt_s, qt_s, A_s, B_s, tid, Tile::THREADS,
+                      warp, Tile::WARPS, lane);
   __syncthreads();
 
   const size_t rec_base = ((size_t)r * p.HV + h) * p.W;  // record position 0
@@ -532,32 +604,28 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   if constexpr (!NATIVE && !BULK) __syncthreads();
 
   // ---- the tiles one after another: C kt_t and C qt_t of every row.  With
-  // ---- bulk copies, tile i sits in buffer i % nbuf, and tile i + nbuf is
-  // ---- requested into it as soon as every warp has moved tile i into
-  // ---- registers.
+  // ---- bulk copies, tile i + 1 is requested into the (single) shared
+  // ---- buffer as soon as every warp has moved tile i into registers.
 #pragma unroll 1
   for (int i = 0; i < NS; ++i) {
     if constexpr (BULK) {
-      const int b = i % nbuf;
-      const uint32_t par = (uint32_t)(i / nbuf) & 1u;
-      const bool ok = mbar_wait(bar + b, par);
-      if (ok) load_tile_shared<K>(s, tbuf + b * kTileElems, warp, l, lr);
+      const bool ok = mbar_wait(bar, i & 1);
+      if (ok) load_tile_shared<K>(s, tbuf, warp, l, lr);
       if (__syncthreads_or(!ok)) {
-        // never expected: report, let the copies in flight land, and stop
+        // never expected: report, let the copy in flight land, and stop
         if (tid == 0 && p.err) atomicOr(p.err, GDN_ROW_ERR_TIMEOUT);
-        for (int j = i; j < NS && j < i + nbuf; ++j) mbar_wait(bar + j % nbuf, (uint32_t)(j / nbuf) & 1u);
+        mbar_wait(bar, i & 1);
         return;
       }
-      if (tid == 0 && i + nbuf < NS) {
+      if (tid == 0 && i + 1 < NS) {
         fence_proxy_async_shared();
-        mbar_expect_tx(bar + b, kTileBytes);
-        bulk_load(tbuf + b * kTileElems, S0 + (size_t)(tile0 + i + nbuf) * VT * K, kTileBytes,
-                  bar + b);
+        mbar_expect_tx(bar, kTileBytes);
+        bulk_load(tbuf, S0 + (size_t)(tile0 + i + 1) * VT * K, kTileBytes, bar);
       }
     } else {
       if (i > 0) load_tile<K, ST, FULL>(s, S0, tile0 + i, p.V, warp, l, lr);
     }
-    tile_products<K>(s, kt_s, qt_s, pq_s, w, SV, i * VT, warp, l, lr);
+    tile_products<K, WC>(s, kt_s, qt_s, pq_s, w, SV, i * VT, warp, l, lr);
   }
   __syncthreads();
 
@@ -566,18 +634,10 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   for (int row = tid; row < SV; row += Tile::THREADS) {
     const int hrow = tile0 * VT + row;  // row of the head
     if (!FULL && hrow >= p.V) continue;
-    float* optr = p.out + t0 * p.out_stride + (size_t)h * p.V + hrow;
-    for (int t = 0; t < w; ++t) {
-      float d = pq_s[(2 * t) * SV + row];
-      for (int j = 0; j < t; ++j) d = __fmaf_rn(A_s[t * p.W + j], u_s[j * SV + row], d);
-      const float u = __fmul_rn(gs_s[4 * t + 1], __fsub_rn(v_s[t * SV + row], d));
-      float o = pq_s[(2 * t + 1) * SV + row];
-      for (int j = 0; j < t; ++j) o = __fmaf_rn(B_s[t * p.W + j], u_s[j * SV + row], o);
-      o = __fmaf_rn(B_s[t * p.W + t], u, o);
-      u_s[t * SV + row] = u;
-      optr[t * p.out_stride] = o;
-      if (!NATIVE) p.rec_u[(rec_base + t) * p.V + hrow] = u;
-    }
+    row_recurrence<WC>(row, w, p.W, SV, pq_s, u_s, gs_s, A_s, B_s,
+                   [&](int t) { return v_s[t * SV + row]; },
+                   p.out + t0 * p.out_stride + (size_t)h * p.V + hrow, p.out_stride,
+                   NATIVE ? nullptr : p.rec_u + rec_base * p.V + hrow, p.V);
   }
 
   // ---- native baseline: fold the tile token by token with the commit's
@@ -617,24 +677,22 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   }
 }
 
-#ifndef GDN_NB_DEFAULT
-#define GDN_NB_DEFAULT 1
-#endif
-
-template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS, bool KDA>
+template <int K, typename QKV, typename ST, bool NATIVE, bool FULL, int NS, bool KDA, int WC = 0>
 static void launch_tiles(const VerifyParams& p, int ntiles, cudaStream_t stream) {
   using Tile = VerifyTile<K>;
   dim3 grid(ntiles / NS, p.HV, p.batch);
-  const int nbuf = NS > 1 ? (GDN_NB_DEFAULT < NS ? GDN_NB_DEFAULT : NS) : 1;
-  const size_t smem = VerifySmem<K, ST, KDA, NATIVE>(p.W, NS).bytes(NS, nbuf);
-  auto kern = gdn_verify_kernel<K, QKV, ST, NATIVE, FULL, NS, KDA>;
+  const size_t smem = VerifySmem<K, ST, KDA, NATIVE>(p.W, NS).bytes(NS);
+  auto kern = gdn_verify_kernel<K, QKV, ST, NATIVE, FULL, NS, KDA, WC>;
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  kern<<<grid, Tile::THREADS, smem, stream>>>(p, nbuf);
+  kern<<<grid, Tile::THREADS, smem, stream>>>(p);
 }
 
 // The verify runs 4 (else 2) tiles of a head per CTA when they divide the
 // head; the native baseline, and heads smaller than a tile, one per CTA.
+// Four tiles with a 4-token record stride (the common draft length: three
+// drafted tokens plus the last accepted one) run a build of the kernel with
+// the token loops unrolled.
 template <int K, typename QKV, typename ST, bool NATIVE, bool KDA>
 static int launch_one(const VerifyParams& p, cudaStream_t stream) {
   using Tile = VerifyTile<K>;
@@ -643,7 +701,8 @@ static int launch_one(const VerifyParams& p, cudaStream_t stream) {
   bool done = false;
   if constexpr (!NATIVE) {
     if (full && ntiles % 4 == 0) {
-      launch_tiles<K, QKV, ST, NATIVE, true, 4, KDA>(p, ntiles, stream);
+      if (p.W == 4) launch_tiles<K, QKV, ST, NATIVE, true, 4, KDA, 4>(p, ntiles, stream);
+      else launch_tiles<K, QKV, ST, NATIVE, true, 4, KDA>(p, ntiles, stream);
       done = true;
     } else if (full && ntiles % 2 == 0) {
       launch_tiles<K, QKV, ST, NATIVE, true, 2, KDA>(p, ntiles, stream);
