@@ -690,9 +690,9 @@ static void launch_tiles(const VerifyParams& p, int ntiles, cudaStream_t stream)
 
 // The verify runs 4 (else 2) tiles of a head per CTA when they divide the
 // head; the native baseline, and heads smaller than a tile, one per CTA.
-// Four tiles with a 4-token record stride (the common draft length: three
-// drafted tokens plus the last accepted one) run a build of the kernel with
-// the token loops unrolled.
+// Four tiles with a 4- or 6-token record stride (three or five drafted
+// tokens plus the last accepted one) run a build of the kernel with the
+// token loops unrolled.
 template <int K, typename QKV, typename ST, bool NATIVE, bool KDA>
 static int launch_one(const VerifyParams& p, cudaStream_t stream) {
   using Tile = VerifyTile<K>;
@@ -702,6 +702,7 @@ static int launch_one(const VerifyParams& p, cudaStream_t stream) {
   if constexpr (!NATIVE) {
     if (full && ntiles % 4 == 0) {
       if (p.W == 4) launch_tiles<K, QKV, ST, NATIVE, true, 4, KDA, 4>(p, ntiles, stream);
+      else if (p.W == 6) launch_tiles<K, QKV, ST, NATIVE, true, 4, KDA, 6>(p, ntiles, stream);
       else launch_tiles<K, QKV, ST, NATIVE, true, 4, KDA>(p, ntiles, stream);
       done = true;
     } else if (full && ntiles % 2 == 0) {
