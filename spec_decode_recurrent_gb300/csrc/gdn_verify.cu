@@ -149,6 +149,17 @@ __device__ __forceinline__ void load_tile(f32x2 (&s)[VerifyTile<K>::RPT][8], con
   }
 }
 
+// The index of the first value a lane holds after LaneHalve<OFF, N> (what
+// LaneHalve accumulates in `base`, without the exchanges).
+template <int OFF, int N>
+struct LaneHalveIndex {
+  static __device__ __forceinline__ int run(int l) {
+    if constexpr (OFF >= 1 && N > 1)
+      return ((l & OFF) != 0 ? N / 2 : 0) + LaneHalveIndex<OFF / 2, N / 2>::run(l);
+    return 0;
+  }
+};
+
 // One token's key and query L2-normalised by a whole warp: lane i < K / 4
 // holds elements 4 i .. 4 i + 3 of each (zeros elsewhere) and writes its
 // four normalised values into khat_row and qhat_row.
@@ -325,8 +336,10 @@ __device__ __forceinline__ void row_recurrence(int row, int w, int W, int SV, co
 
 // Per token: the tile's rows against kt_t and qt_t, summed over each row's
 // lanes, into pq_s[t][0 / 1][row0 + row].  Value v = 2 g + which of a lane
-// is row group g's C kt (which 0) or C qt (which 1).  WC > 0: at most WC
-// tokens, the token loop unrolled.
+// is row group g's C kt (which 0) or C qt (which 1).  Which values a lane
+// ends with, and where they go, is fixed per lane and worked out once.
+// WC > 0: at most WC tokens, the token loop unrolled by two (fully unrolled
+// it measured slower).
 template <int K, int WC>
 __device__ __forceinline__ void tile_products(const f32x2 (&s)[VerifyTile<K>::RPT][8],
                                               const float* kt_s, const float* qt_s, float* pq_s,
@@ -337,6 +350,14 @@ __device__ __forceinline__ void tile_products(const f32x2 (&s)[VerifyTile<K>::RP
   constexpr int NSTEP = LPR < NV ? LPR : NV;        // lanes the halving spans
   constexpr int NR = NV / NSTEP;                    // values left per lane
   constexpr int DUP = LPR / NSTEP - 1;              // lane bits holding copies
+  const int base = LaneHalveIndex<LPR / 2, NV>::run(l);
+  const bool writer = (l & DUP) == 0;
+  int wofs[NR];  // the lane's values' offsets in pq_s for token 0
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int v = base + i, g = v >> 1, which = v & 1;
+    wofs[i] = which * SV + row0 + (g * Tile::WARPS + warp) * RPW + lr;
+  }
   auto token = [&](int t) {
     f32x2 kk[8], qq[8];
 #pragma unroll
@@ -364,18 +385,15 @@ __device__ __forceinline__ void tile_products(const f32x2 (&s)[VerifyTile<K>::RP
       x[2 * g] = __fadd_rn(dd.x, dd.y);
       x[2 * g + 1] = __fadd_rn(oo.x, oo.y);
     }
-    int base = 0;
-    LaneHalve<LPR / 2, NV>::run(x, l, base);
-    if ((l & DUP) == 0) {
+    int ignored = 0;  // the same index as `base`
+    LaneHalve<LPR / 2, NV>::run(x, l, ignored);
+    if (writer) {
 #pragma unroll
-      for (int i = 0; i < NR; ++i) {
-        const int v = base + i, g = v >> 1, which = v & 1;
-        pq_s[(2 * t + which) * SV + row0 + (g * Tile::WARPS + warp) * RPW + lr] = x[i];
-      }
+      for (int i = 0; i < NR; ++i) pq_s[2 * t * SV + wofs[i]] = x[i];
     }
   };
   if constexpr (WC > 0) {
-#pragma unroll
+#pragma unroll 2
     for (int t = 0; t < WC; ++t)
       if (t < w) token(t);
   } else {
