@@ -17,7 +17,7 @@
 // token in a serial chain.  The window's side (kt, qt, A, B: O(w^2 K)) is
 // computed once per CTA.
 //
-// One CTA of 4 warps covers up to four tiles of VT state rows (32 for
+// One CTA of 4 warps covers up to four tiles of VT state rows (64 for
 // K = 128) of one (request row, value head), the tile held in registers, a
 // cooperative 4-warp CTA per 128x128 state head (tokenspeed PR,
 // Implementation).  Per tile and token each lane forms its partial products
@@ -26,7 +26,7 @@
 // other half), and the row sums land in shared memory.  After the last tile
 // one thread per row runs the short scalar recurrence for u_t and o_t and
 // writes both, coalesced.  Tiles reach the CTA as single bulk copies
-// (cp.async.bulk, one thread per 16 KiB tile) into a shared buffer, completed
+// (cp.async.bulk, one thread per 32 KiB tile) into a shared buffer, completed
 // through an mbarrier; tile i + 1 is requested as soon as every warp has
 // moved tile i into registers.
 //
@@ -49,13 +49,19 @@ template <int K>
 struct VerifyTile {
   static constexpr int LPR = K / 16;              // lanes per state row
   static constexpr int RPW = 32 / LPR;            // rows per warp per row group
-  static constexpr int RPT = (K == 128) ? 2 : 1;  // row groups per thread
+  // four row groups per thread at K = 128: each token's key and query
+  // values a lane reads from shared memory serve four rows (two measured
+  // slower: the shared-memory data pipe was the busiest unit)
+  static constexpr int RPT = (K == 128) ? 4 : 1;  // row groups per thread
   static constexpr int WARPS = 4;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int VT = WARPS * RPW * RPT;    // state rows per tile
+  // CTAs per SM the registers must allow: four at K = 128 (four row groups
+  // per thread, about 110 registers); otherwise six (80 registers) for the
+  // verify with an fp32 state and seven (72) for the rest
   template <bool NATIVE, typename ST, bool KDA>
   static constexpr int min_ctas() {
-    return (!NATIVE && sizeof(ST) == 4) ? 6 : 7;
+    return K == 128 ? 4 : ((!NATIVE && sizeof(ST) == 4) ? 6 : 7);
   }
 };
 
@@ -724,7 +730,9 @@ static int launch_one(const VerifyParams& p, cudaStream_t stream) {
       else launch_tiles<K, QKV, ST, NATIVE, true, 4, KDA>(p, ntiles, stream);
       done = true;
     } else if (full && ntiles % 2 == 0) {
-      launch_tiles<K, QKV, ST, NATIVE, true, 2, KDA>(p, ntiles, stream);
+      if (p.W == 4) launch_tiles<K, QKV, ST, NATIVE, true, 2, KDA, 4>(p, ntiles, stream);
+      else if (p.W == 6) launch_tiles<K, QKV, ST, NATIVE, true, 2, KDA, 6>(p, ntiles, stream);
+      else launch_tiles<K, QKV, ST, NATIVE, true, 2, KDA>(p, ntiles, stream);
       done = true;
     }
   }
