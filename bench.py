@@ -243,6 +243,11 @@ COMMIT_SOURCES = ["spec_decode_recurrent_gb300/csrc/gdn_commit.cu",
                   "spec_decode_recurrent_gb300/csrc/gdn_device.cuh",
                   "spec_decode_recurrent_gb300/csrc/gdn_async.cuh"]
 VERIFY_SOURCES = ["spec_decode_recurrent_gb300/csrc/gdn_verify.cu",
+                  "spec_decode_recurrent_gb300/csrc/gdn_verify_impl.cuh",
+                  "spec_decode_recurrent_gb300/csrc/gdn_verify_k128.cu",
+                  "spec_decode_recurrent_gb300/csrc/gdn_verify_k128_kda.cu",
+                  "spec_decode_recurrent_gb300/csrc/gdn_verify_k64.cu",
+                  "spec_decode_recurrent_gb300/csrc/gdn_verify_k16_k32.cu",
                   "spec_decode_recurrent_gb300/csrc/gdn_device.cuh",
                   "spec_decode_recurrent_gb300/csrc/gdn_async.cuh"]
 

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libgdn_spec.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-SOURCES = ["gdn_verify.cu", "gdn_commit.cu", "gdn_conv.cu", "gdn_abi.cu"]
+SOURCES = ["gdn_verify_k128.cu", "gdn_verify_k128_kda.cu", "gdn_verify_k64.cu", "gdn_verify_k16_k32.cu",
+           "gdn_verify.cu", "gdn_commit.cu", "gdn_conv.cu", "gdn_abi.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -1,0 +1,11 @@
+// gdn_verify_k128_kda.cu -- verify and native-snapshot kernels for head width 128, per-channel (KDA) decay.
+#include "gdn_verify_impl.cuh"
+
+namespace gdn {
+
+int launch_verify_k128_kda(const VerifyParams& p, int qkv_dtype, int state_dtype, bool native,
+                          cudaStream_t stream) {
+  return dispatch_native<128, true>(p, qkv_dtype, state_dtype, native, stream);
+}
+
+}  // namespace gdn
