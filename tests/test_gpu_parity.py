@@ -50,7 +50,7 @@ def test_tiny_config_full_oracle():
 
 
 SMALL = {
-    # several 32-row tiles, ragged windows incl. decode-only (1) and padding (0),
+    # two 64-row tiles per head, ragged windows incl. decode-only (1) and padding (0),
     # a null-slot row, strided fused q/k/v, permuted rows with gaps
     "ragged_fp32": dict(HK=2, HV=4, K=128, V=128, W=6, L=2, windows=[6, 4, 1, 3, 0, 6, 2],
                         accepted=[3, 4, 1, 2, 0, 6, 1], null_rows=(5,), gaps=[1, 0, 2, 3, 0, 1, 0],
@@ -79,11 +79,18 @@ SMALL = {
                                  accepted=[16, 13, 9, 12], block_size=4, seq_pos=[5, 8, 3, 1]),
     "align_block3_w6": dict(HK=1, HV=2, K=64, V=64, W=6, L=2, windows=[6, 6, 6, 3],
                             accepted=[6, 5, 3, 3], block_size=3, seq_pos=[1, 2, 3, 7]),
-    # two 32-row tiles per verify CTA (K = 128, V = 64), fp32 and bf16 state
+    # a head of one 64-row tile (K = 128, V = 64): the verify's one-tile path,
+    # fp32 and bf16 state
     "two_tile_span": dict(HK=1, HV=2, K=128, V=64, W=5, L=2, windows=[5, 2, 1, 5],
                           accepted=[3, 2, 1, 5], qkv_dtype=wl.BF16),
     "two_tile_span_bf16_state": dict(HK=1, HV=2, K=128, V=64, W=4, L=1, windows=[4, 3, 4],
                                      accepted=[2, 3, 4], qkv_dtype=wl.BF16, state_dtype=wl.BF16),
+    # four 32-row tiles per verify CTA (K = 64, V = 128): the 4-token build
+    # and the generic one
+    "k64_v128_four_tiles": dict(HK=1, HV=2, K=64, V=128, W=4, L=2, windows=[4, 3, 4],
+                                accepted=[2, 3, 4], qkv_dtype=wl.BF16),
+    "k64_v128_four_tiles_w5": dict(HK=1, HV=2, K=64, V=128, W=5, L=1, windows=[5, 2],
+                                   accepted=[5, 1]),
     # bf16 states at narrow heads: the shared-memory-staged commit with a
     # tile taller than the head (ragged) and with two row tiles
     "k64_bf16_state": dict(HK=2, HV=4, K=64, V=64, W=4, L=2, windows=[4, 1, 4],
