@@ -29,7 +29,8 @@
 // other half), and the row sums land in shared memory.  After the last tile
 // one thread per row runs the short scalar recurrence for u_t and o_t and
 // writes both, coalesced.  Tiles reach the CTA as single bulk copies
-// (cp.async.bulk, one thread per 32 KiB tile) into a shared buffer, completed
+// (cp.async.bulk, one thread per tile: 32 KiB for a 64 x 128 fp32 tile)
+// into a shared buffer, completed
 // through an mbarrier; tile i + 1 is requested as soon as every warp has
 // moved tile i into registers.
 //
