@@ -107,3 +107,37 @@ def test_kda_commit_skips_rows_the_verify_rejected():
     bad = int(sb.slot_table[1, 0])
     assert torch.equal(bits(sb.pools[0][bad]), bits(gs.before[0][bad]))
     assert torch.equal(gs.bufs.rec_g[0][1, :, 0, 0].cpu(), torch.full((sb.HV,), -1.0))
+
+
+@pytest.mark.parametrize("kda", [False, True])
+@pytest.mark.parametrize("qkv_dtype", [wl.F32, wl.BF16])
+def test_value_and_gate_rows_off_the_16_byte_grid(kda, qkv_dtype):
+    # The library asks only element alignment of v (and 4 bytes of the KDA
+    # gate inputs); the verify stages 16-byte pieces where rows allow it and
+    # single elements elsewhere.  The same step with every value row and
+    # gate input moved off the 16-byte grid must give the same bits.
+    kw = dict(HK=1, HV=2, K=128, V=128, W=4, L=1, windows=[4, 3, 4], accepted=[2, 3, 4],
+              qkv_dtype=qkv_dtype, kda=kda)
+    ref = wl.custom(device="cuda", **kw)
+    odd = wl.custom(device="cuda", **kw)
+    T, HV, V = odd.v[0].shape
+    buf = torch.empty((T, HV * V + 1), dtype=odd.v[0].dtype, device="cuda")
+    v = buf[:, 1:].unflatten(1, (HV, V))      # odd row stride, base one element in
+    v.copy_(odd.v[0])
+    odd.v[0] = v
+    assert v.stride(0) % 2 == 1
+    if kda:
+        def shifted(x):
+            flat = torch.empty(x.numel() + 1, dtype=x.dtype, device="cuda")
+            y = flat[1:].view(x.shape)        # 4 bytes off the 16-byte grid
+            y.copy_(x)
+            return y
+        odd.a[0] = shifted(odd.a[0])
+        odd.dt_bias[0] = shifted(odd.dt_bias[0])
+        assert odd.a[0].data_ptr() % 16 != 0 and odd.dt_bias[0].data_ptr() % 16 != 0
+    g_ref, g_odd = GpuStep(ref), GpuStep(odd)
+    assert g_ref.err == 0 and g_odd.err == 0
+    for name in ("out", "rec_u", "rec_k", "rec_g"):
+        assert torch.equal(bits(getattr(g_ref.bufs, name)[0]), bits(getattr(g_odd.bufs, name)[0])), name
+    assert torch.equal(bits(ref.pools[0]), bits(odd.pools[0]))
+    g_odd.check_bitwise()
