@@ -44,6 +44,9 @@ SMALL = {
     "k32_v64_two_tiles": dict(HK=1, HV=2, K=32, V=128, W=3, L=1, windows=[3, 2], accepted=[1, 2]),
     "k16_v16": dict(HK=2, HV=2, K=16, V=16, W=4, L=1, windows=[4, 4], accepted=[1, 3]),
     "max_window16": dict(HK=1, HV=2, K=128, V=128, W=16, L=1, windows=[16, 9], accepted=[16, 7]),
+    # every window length under the unrolled 4-token build
+    "w4_every_window": dict(HK=1, HV=2, K=128, V=128, W=4, L=1, windows=[1, 2, 3, 4],
+                            accepted=[1, 2, 1, 3], qkv_dtype=wl.BF16),
 }
 
 

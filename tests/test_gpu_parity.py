@@ -104,6 +104,9 @@ SMALL = {
     "k16_bf16_state_align": dict(HK=1, HV=1, K=16, V=32, W=6, L=1, windows=[6, 6],
                                  accepted=[6, 4], block_size=2, seq_pos=[2, 5],
                                  state_dtype=wl.BF16),
+    # every window length under the unrolled 4-token build
+    "w4_every_window": dict(HK=1, HV=2, K=128, V=128, W=4, L=1, windows=[1, 2, 3, 4],
+                            accepted=[1, 2, 1, 3], qkv_dtype=wl.BF16),
 }
 
 
