@@ -428,6 +428,10 @@ __global__ void __launch_bounds__(VerifyTile<K>::THREADS,
   static_assert(!NATIVE || NS == 1, "the native form runs one tile per CTA");
   extern __shared__ __align__(16) unsigned char smem_raw[];
 
+  // launched as a programmatic dependent of the previous kernel in the
+  // stream: nothing is read before that kernel has completed and its
+  // writes are visible (only the launch itself overlaps its tail)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int span = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile0 = span * NS;  // first tile of this CTA
@@ -715,7 +719,20 @@ static void launch_tiles(const VerifyParams& p, int ntiles, cudaStream_t stream)
   auto kern = gdn_verify_kernel<K, QKV, ST, NATIVE, FULL, NS, KDA, WC>;
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  kern<<<grid, Tile::THREADS, smem, stream>>>(p);
+  // programmatic stream serialization: the CTAs may be launched while the
+  // previous kernel's last CTAs run; each waits for it at its first
+  // instruction (the launch latency of back-to-back layers overlaps)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(Tile::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 // The verify runs 4 (else 2) tiles of a head per CTA when they divide the
