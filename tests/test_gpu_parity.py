@@ -335,3 +335,29 @@ def test_verify_writes_into_a_strided_output_view(kda):
     assert torch.isnan(wide[:, sb.HV * sb.V:]).all()
     for name in ("rec_u", "rec_k", "rec_g"):
         assert torch.equal(bits(getattr(bufs, name)[0]), bits(getattr(ref, name)[0]))
+
+
+@pytest.mark.parametrize("kda", [False, True])
+def test_verify_reads_inputs_the_previous_kernel_wrote(kda):
+    # The verify is launched as a programmatic dependent of the stream's
+    # previous kernel: its CTAs may start while that kernel's last CTAs run,
+    # and must not read before it has finished.  Here the previous kernels
+    # rewrite every input of the step (after a scramble) right before each
+    # verify; the outputs must be the reference ones every time.
+    sb = wl.custom(device="cuda", kda=kda, HK=2, HV=4, K=128, V=128, W=4, L=1,
+                   windows=[4, 3, 4, 2], accepted=[2, 3, 4, 1], qkv_dtype=wl.BF16)
+    ref = step.StepBuffers(sb, fill=float("nan"))
+    step.verify_all(sb, ref)
+    torch.cuda.synchronize()
+    inputs = [sb.q[0], sb.k[0], sb.v[0], sb.a[0], sb.b[0]]
+    saved = [x.clone() for x in inputs]
+    for _ in range(20):
+        bufs = step.StepBuffers(sb, fill=float("nan"))
+        for x in inputs:
+            x.fill_(7.0)
+        for x, y in zip(inputs, saved):
+            x.copy_(y)
+        step.verify_all(sb, bufs)
+        torch.cuda.synchronize()
+        for name in ("out", "rec_u", "rec_k", "rec_g"):
+            assert torch.equal(bits(getattr(ref, name)[0]), bits(getattr(bufs, name)[0])), name
